@@ -1,0 +1,28 @@
+"""CPU oracle for fine-grained FP8 quantisation and the block-scaled FP8 GEMM.
+
+TEST INFRASTRUCTURE ONLY.  Plain numpy, float64/int64 where precision matters,
+written from the DeepSeek-V3 FP8 training passages on the five scraped pages
+(cited per function as page + passage/figure; the page names are listed in
+the design notes).  It shares no code, header, table or constant generator
+with the CUDA library, and the CUDA library never imports it.  Only the tests,
+the smoke check and the benchmark's CPU-baseline leg may call it.
+
+Pins (checked in tests/test_oracle_*.py without a GPU):
+  e4m3   exhaustive over all 256 codes; round-trip; monotonicity; every
+         midpoint ties to even; structured float32 sweeps against two library
+         casts (ml_dtypes, torch); saturation.
+  quant  amax maps to +-448 exactly; power-of-2 scale rule; error bound of
+         one E4M3 half-ulp times the tile amax; a hand-worked tile fixture;
+         transposed mode equals quantising the transpose.
+  gemm   brute force in exact rationals on tiny shapes; int64 per-slice sums;
+         special cases that reduce to a library matmul; scale linearity;
+         Dgrad/Wgrad transposition identities.
+  group  E=1 equals dense; empty experts; relabelling invariance.
+Parity unpinned: the "about 2% error at K=4096 with ~14-bit accumulation"
+figure (no mechanism detail to reproduce it); it is context only.
+"""
+
+from .e4m3 import E4M3_MAX, decode, encode  # noqa: F401
+from .quant import (act_quant, act_quant_t, weight_quant, dequant_tiles,  # noqa: F401
+                    dequant_blocks, scale_from_amax)
+from .scaled_gemm import gemm, grouped_gemm, slice_partials  # noqa: F401

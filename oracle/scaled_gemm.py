@@ -1,0 +1,91 @@
+"""Block-scaled FP8 GEMM with per-128-K promotion.  TEST INFRASTRUCTURE ONLY.
+
+Definition (page 2, inprokorea.com free #735329: the promotion passage and
+Figure 6, and the per-group-scaling passage): the K dimension is cut into
+groups of 128; each group's partial product of the E4M3 operands is formed,
+multiplied by that group's activation-tile scale and weight-block scale, and
+added into a full-precision accumulator:
+
+    C[m, n] = sum_kb  P_kb[m, n] * sa[m, kb] * sb(n, kb),
+    P_kb[m, n] = sum_{k in group kb} decode(A[m, k]) * decode(B[n, k])
+
+with sb(n, kb) = sb[n // 128, kb] for 128x128 weight blocks, or sb[n, kb] when
+B also carries 1x128 tiles (the Wgrad case, both operands quantised along the
+token dimension; page 5, inprokorea.com free #890463, backward-pass passage).
+
+Exactness: every E4M3 value is an integer multiple of 2^-9 below 2^9 in
+magnitude, so 2^18 * P_kb is an integer below 2^43 and any float64 summation
+order (BLAS included) gives P_kb exactly.  sa*sb is exact in float64 (24+24
+bits).  The only roundings are the float64 products with P_kb and the float64
+sum over groups.  Output dtype rounding (BF16 / FP32) is the caller's.
+"""
+
+from __future__ import annotations
+
+import numpy as np
+
+from .e4m3 import decode
+
+TILE = 128
+
+
+def slice_partials(qa, qb) -> np.ndarray:
+    """All P_kb at once: float64 [K/128, M, N] (exact)."""
+    A = decode(qa)
+    B = decode(qb)
+    K = A.shape[1]
+    nkb = K // TILE
+    out = np.empty((nkb, A.shape[0], B.shape[0]), dtype=np.float64)
+    for kb in range(nkb):
+        sl = slice(kb * TILE, (kb + 1) * TILE)
+        out[kb] = A[:, sl] @ B[:, sl].T
+    return out
+
+
+def _b_scale(sb, n_rows: int, kb: int, b_tile: bool) -> np.ndarray:
+    sb = np.asarray(sb, dtype=np.float64)
+    if b_tile:
+        return sb[:, kb]
+    return np.repeat(sb[:, kb], TILE)[:n_rows]
+
+
+def gemm(qa, sa, qb, sb, b_tile: bool = False) -> np.ndarray:
+    """float64 C[M, N] for A codes [M, K], B codes [N, K] (both K-major).
+
+    sa: float32 [M, K/128]; sb: float32 [N/128, K/128] (blocks) or [N, K/128]
+    (b_tile=True).
+    """
+    qa = np.asarray(qa)
+    qb = np.asarray(qb)
+    M, K = qa.shape
+    N, Kb = qb.shape
+    if K != Kb or K % TILE:
+        raise ValueError("bad K")
+    A = decode(qa)
+    B = decode(qb)
+    sa = np.asarray(sa, dtype=np.float64)
+    C = np.zeros((M, N), dtype=np.float64)
+    for kb in range(K // TILE):
+        sl = slice(kb * TILE, (kb + 1) * TILE)
+        P = A[:, sl] @ B[:, sl].T
+        C += P * (sa[:, kb][:, None] * _b_scale(sb, N, kb, b_tile)[None, :])
+    return C
+
+
+def grouped_gemm(qa, sa, offsets, qb, sb) -> np.ndarray:
+    """Per-expert gemm over contiguous row groups.
+
+    qa [T, K], sa [T, K/128]; offsets int [E+1] (non-decreasing, 0..T);
+    qb [E, N, K]; sb [E, N/128, K/128].  Rows of expert e are
+    offsets[e]..offsets[e+1]-1 and use B[e] only.
+    """
+    qa = np.asarray(qa)
+    off = np.asarray(offsets, dtype=np.int64)
+    E = off.shape[0] - 1
+    N = qb.shape[1]
+    C = np.zeros((qa.shape[0], N), dtype=np.float64)
+    for e in range(E):
+        r0, r1 = int(off[e]), int(off[e + 1])
+        if r1 > r0:
+            C[r0:r1] = gemm(qa[r0:r1], np.asarray(sa)[r0:r1], qb[e], sb[e])
+    return C

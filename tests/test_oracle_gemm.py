@@ -1,0 +1,220 @@
+"""Pins for the oracle's block-scaled GEMM and grouped GEMM (CPU only).
+
+The definition (page 2, inprokorea.com free #735329, promotion passage and
+Figure 6; per-group scaling passage): partial products over each 128-wide K
+group are scaled by that group's activation and weight scales and accumulated
+at full precision.  Pinned here by exact rational brute force, by an int64
+restatement of the partial sums, and by special cases that reduce to a
+library matmul.
+"""
+
+from fractions import Fraction
+
+import numpy as np
+import pytest
+
+import oracle
+from oracle import e4m3
+from oracle import scaled_gemm as og
+
+FINITE = np.array([c for c in range(256) if (c & 0x7F) != 0x7F], dtype=np.uint8)
+
+
+def _codes(shape, g):
+    return g.choice(FINITE, size=shape)
+
+
+def _scales(shape, g):
+    return np.exp(g.uniform(-20, 20, shape)).astype(np.float32)
+
+
+def _exact(qa, sa, qb, sb, b_tile):
+    """C as exact rationals: sum over groups of (sum of products) * sa * sb."""
+    M, K = qa.shape
+    N = qb.shape[0]
+    A = [[Fraction(float(v)) for v in row] for row in e4m3.decode(qa)]
+    B = [[Fraction(float(v)) for v in row] for row in e4m3.decode(qb)]
+    C = [[Fraction(0)] * N for _ in range(M)]
+    mag = np.zeros((M, N))
+    for m in range(M):
+        for n in range(N):
+            acc = Fraction(0)
+            tot = 0.0
+            for kb in range(K // 128):
+                p = sum(A[m][k] * B[n][k] for k in range(kb * 128, kb * 128 + 128))
+                sbv = sb[n, kb] if b_tile else sb[n // 128, kb]
+                term = p * Fraction(float(sa[m, kb])) * Fraction(float(sbv))
+                acc += term
+                tot += abs(float(term))
+            C[m][n] = acc
+            mag[m, n] = tot
+    return C, mag
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 1, 128), (2, 3, 128), (3, 2, 256), (3, 3, 384)])
+@pytest.mark.parametrize("b_tile", [False, True])
+def test_bruteforce_rational(M, N, K, b_tile):
+    g = np.random.default_rng(M * 100 + N * 10 + K + b_tile)
+    qa, qb = _codes((M, K), g), _codes((N, K), g)
+    sa = _scales((M, K // 128), g)
+    sb = _scales((N, K // 128) if b_tile else ((N + 127) // 128, K // 128), g)
+    C = oracle.gemm(qa, sa, qb, sb, b_tile=b_tile)
+    exact, mag = _exact(qa, sa, qb, sb, b_tile)
+    for m in range(M):
+        for n in range(N):
+            err = abs(Fraction(float(C[m, n])) - exact[m][n])
+            assert float(err) <= 2.0 ** -50 * mag[m, n], (m, n)
+
+
+def test_slice_partials_are_exact_integers():
+    g = np.random.default_rng(11)
+    qa, qb = _codes((17, 512), g), _codes((9, 512), g)
+    P = og.slice_partials(qa, qb)
+    ia = np.rint(e4m3.decode(qa) * 512).astype(np.int64)      # codes are multiples of 2^-9
+    ib = np.rint(e4m3.decode(qb) * 512).astype(np.int64)
+    for kb in range(4):
+        sl = slice(kb * 128, kb * 128 + 128)
+        ref = ia[:, sl] @ ib[:, sl].T                          # int64, |.| < 2^43
+        assert np.array_equal(P[kb] * 2.0 ** 18, ref.astype(np.float64))
+        assert np.all(np.abs(ref) < 2 ** 43)
+
+
+def test_unit_scales_small_integers_reduce_to_int_matmul():
+    g = np.random.default_rng(12)
+    ints = g.integers(-16, 17, size=(40, 384))
+    intsb = g.integers(-16, 17, size=(256, 384))
+    qa = e4m3.encode(ints.astype(np.float32))                  # |i| <= 16 is exact in E4M3
+    qb = e4m3.encode(intsb.astype(np.float32))
+    assert np.array_equal(e4m3.decode(qa), ints)
+    C = oracle.gemm(qa, np.ones((40, 3), np.float32), qb, np.ones((2, 3), np.float32))
+    assert np.array_equal(C, (ints @ intsb.T).astype(np.float64))
+
+
+def test_single_group_equals_dequantised_matmul():
+    g = np.random.default_rng(13)
+    x = g.standard_normal((50, 128)).astype(np.float32)
+    w = (g.standard_normal((256, 128)) * 0.02).astype(np.float32)
+    qa, sa = oracle.act_quant(x)
+    qb, sb = oracle.weight_quant(w)
+    C = oracle.gemm(qa, sa, qb, sb)
+    ref = oracle.dequant_tiles(qa, sa) @ oracle.dequant_blocks(qb, sb).T
+    np.testing.assert_allclose(C, ref, rtol=1e-13, atol=1e-13 * np.abs(ref).max())
+
+
+def test_multi_group_equals_dequantised_matmul_to_rounding():
+    g = np.random.default_rng(14)
+    x = g.standard_normal((64, 1024)).astype(np.float32)
+    w = g.standard_normal((128, 1024)).astype(np.float32)
+    qa, sa = oracle.act_quant(x)
+    qb, sb = oracle.weight_quant(w)
+    C = oracle.gemm(qa, sa, qb, sb)
+    ref = oracle.dequant_tiles(qa, sa) @ oracle.dequant_blocks(qb, sb).T
+    assert np.linalg.norm(C - ref) <= 1e-13 * np.linalg.norm(ref)
+    # and the quantised product tracks the unquantised one at E4M3 accuracy
+    full = x.astype(np.float64) @ w.astype(np.float64).T
+    assert np.linalg.norm(C - full) / np.linalg.norm(full) < 0.05
+
+
+def test_power_of_two_scale_is_linear_and_exact():
+    g = np.random.default_rng(15)
+    qa, qb = _codes((6, 256), g), _codes((128, 256), g)
+    sa, sb = _scales((6, 2), g), _scales((1, 2), g)
+    C = oracle.gemm(qa, sa, qb, sb)
+    sa2 = sa.copy()
+    sa2[3] *= 2
+    C2 = oracle.gemm(qa, sa2, qb, sb)
+    assert np.array_equal(C2[3], 2 * C[3])
+    assert np.array_equal(np.delete(C2, 3, 0), np.delete(C, 3, 0))
+
+
+def test_block_mode_equals_tile_mode_with_repeated_scales():
+    g = np.random.default_rng(16)
+    qa, qb = _codes((5, 384), g), _codes((256, 384), g)
+    sa, sb = _scales((5, 3), g), _scales((2, 3), g)
+    Cb = oracle.gemm(qa, sa, qb, sb)
+    Ct = oracle.gemm(qa, sa, qb, np.repeat(sb, 128, axis=0), b_tile=True)
+    assert np.array_equal(Cb, Ct)
+
+
+def test_wgrad_transpose_identity():
+    # tile x tile scaling is symmetric: (A B^T)^T == B A^T exactly
+    g = np.random.default_rng(17)
+    qa, qb = _codes((7, 256), g), _codes((11, 256), g)
+    sa, sb = _scales((7, 2), g), _scales((11, 2), g)
+    assert np.array_equal(oracle.gemm(qa, sa, qb, sb, b_tile=True).T,
+                          oracle.gemm(qb, sb, qa, sa, b_tile=True))
+
+
+def test_dgrad_via_transposed_weight_codes():
+    # Dgrad uses W^T's codes/scales (exact transposes of the block quantisation)
+    g = np.random.default_rng(18)
+    dy = g.standard_normal((8, 256)).astype(np.float32)
+    w = g.standard_normal((256, 384)).astype(np.float32)       # [N_out, K_in]
+    qw, sw, qwt, swt = oracle.weight_quant(w, transposed=True)
+    qd, sd = oracle.act_quant(dy)
+    C = oracle.gemm(qd, sd, qwt, swt)                         # dX = dY . W  ([8, 384])
+    ref = oracle.dequant_tiles(qd, sd) @ oracle.dequant_blocks(qw, sw)
+    assert np.linalg.norm(C - ref) <= 1e-13 * np.linalg.norm(ref)
+
+
+def test_grouped_single_expert_equals_dense():
+    g = np.random.default_rng(19)
+    qa, qb = _codes((40, 256), g), _codes((1, 128, 256), g)
+    sa, sb = _scales((40, 2), g), _scales((1, 1, 2), g)
+    C = oracle.grouped_gemm(qa, sa, np.array([0, 40]), qb, sb)
+    assert np.array_equal(C, oracle.gemm(qa, sa, qb[0], sb[0]))
+
+
+def test_grouped_empty_experts_and_relabelling():
+    g = np.random.default_rng(20)
+    sizes = [3, 0, 5, 0, 1]
+    off = np.concatenate([[0], np.cumsum(sizes)])
+    T = off[-1]
+    qa, sa = _codes((T, 256), g), _scales((T, 2), g)
+    qb, sb = _codes((5, 128, 256), g), _scales((5, 1, 2), g)
+    C = oracle.grouped_gemm(qa, sa, off, qb, sb)
+    for e in range(5):
+        r0, r1 = off[e], off[e + 1]
+        if r1 > r0:
+            assert np.array_equal(C[r0:r1], oracle.gemm(qa[r0:r1], sa[r0:r1], qb[e], sb[e]))
+    # relabel experts: reverse their order and move their rows with them
+    perm = [4, 3, 2, 1, 0]
+    rows = np.concatenate([np.arange(off[e], off[e + 1]) for e in perm]).astype(int)
+    off2 = np.concatenate([[0], np.cumsum([sizes[e] for e in perm])])
+    C2 = oracle.grouped_gemm(qa[rows], sa[rows], off2, qb[perm], sb[perm])
+    assert np.array_equal(C2, C[rows])
+
+
+def test_grouped_bruteforce_rational():
+    g = np.random.default_rng(21)
+    off = np.array([0, 2, 2, 3])
+    qa, sa = _codes((3, 128), g), _scales((3, 1), g)
+    qb, sb = _codes((3, 2, 128), g), _scales((3, 1, 1), g)
+    C = oracle.grouped_gemm(qa, sa, off, qb, sb)
+    for e in range(3):
+        r0, r1 = off[e], off[e + 1]
+        if r1 == r0:
+            continue
+        ex, mag = _exact(qa[r0:r1], sa[r0:r1], qb[e], sb[e], False)
+        for i in range(r1 - r0):
+            for n in range(2):
+                assert float(abs(Fraction(float(C[r0 + i, n])) - ex[i][n])) <= 2.0 ** -50 * mag[i, n]
+
+
+def test_planted_mistakes_are_caught(monkeypatch):
+    """A wrong scale index or a transposed operand in the oracle trips the brute force."""
+    real = og._b_scale
+
+    def wrong_group(sb, n_rows, kb, b_tile):           # uses the next group's scale
+        nkb = np.asarray(sb).shape[1]
+        return real(sb, n_rows, (kb + 1) % nkb, b_tile)
+
+    monkeypatch.setattr(og, "_b_scale", wrong_group)
+    with pytest.raises(AssertionError):
+        test_bruteforce_rational(3, 2, 256, False)
+    monkeypatch.setattr(og, "_b_scale", real)
+
+    real_decode = og.decode
+    monkeypatch.setattr(og, "decode", lambda c: -real_decode(c) if np.asarray(c).shape[0] == 2 else real_decode(c))
+    with pytest.raises(AssertionError):
+        test_bruteforce_rational(3, 2, 256, True)
