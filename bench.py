@@ -1,0 +1,414 @@
+#!/usr/bin/env python3
+"""Benchmark of the fine-grained FP8 hot path on B300.
+
+One step = one pass of the FP8 Linear forward at the DeepSeek-V3 FFN shape:
+  act_quant   X[4096, 7168] BF16 -> E4M3 codes + 1x128 FP32 scales
+  weight_quant W[18432, 7168] BF16 -> E4M3 codes + 128x128 FP32 scales
+  gemm        codes -> C[4096, 18432] BF16, FP32 promotion every 128 K
+Inputs are seeded synthetic BF16 tensors already resident in HBM.  The
+per-step working set (~0.66 GB) is far larger than L2 (126 MB).
+
+value = GEMM FLOPs of all steps on all ranks / max-over-ranks wall time of
+the timed region (CUDA events), i.e. effective TFLOP/s of the whole step with
+its quantisation included.  The per-kernel numbers (GEMM TFLOP/s, act_quant
+GB/s) are in "per_op" and "roofline".
+
+--impl reference times the CPU oracle on a bounded sample of the same step
+and extrapolates to the full step.  Multi-GPU runs are independent replicas
+(weak scaling; this path has no data exchange).
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "FP8 block-scaled GEMM TFLOP/s (% FP8 peak); act_quant GB/s (% HBM) on 1 B300"
+M, N, K = 4096, 18432, 7168
+FLOPS = 2 * M * N * K
+WORKLOAD = "fprop_ffn_x4096x7168_w18432x7168"
+GEMM_SOURCES = ["fp8_fine_grained_19_b300/csrc/gemm.cu",
+                "fp8_fine_grained_19_b300/csrc/device_common.cuh"]
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "gemm_fprop_traffic.json")
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=200)
+    p.add_argument("--warmup", type=int, default=10)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--e2e-steps", type=int, default=20)
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-e2e", action="store_true")
+    return p.parse_args()
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        d = json.load(open(path))
+        return dict(hbm_gbs=float(d["hbm_gbs"]), bf16=float(d["bf16_tflops"]),
+                    bf16_sustained=float(d.get("bf16_tflops_sustained", d["bf16_tflops"])),
+                    source="measured")
+    except Exception:
+        return dict(hbm_gbs=6400.0, bf16=1800.0, bf16_sustained=1400.0, source="fallback")
+
+
+def src_hash(paths) -> str:
+    h = hashlib.sha256()
+    for p in paths:
+        h.update(open(os.path.join(ROOT, p), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def traffic_for_current_kernel():
+    """DRAM bytes per GEMM launch from the committed ncu capture, if the kernel is unchanged."""
+    try:
+        d = json.load(open(TRAFFIC_FILE))
+    except Exception:
+        return None
+    if d.get("source_hash") != src_hash(GEMM_SOURCES):
+        return None
+    return d.get("bytes_per_launch_full_size")
+
+
+# ----------------------------------------------------------------- clocks
+class ClockSampler:
+    """Polls NVML (SM clock, power, throttle reasons) on a thread during the timed region."""
+
+    def __init__(self, device_index: int, period_s: float = 0.005):
+        self.samples = []
+        self.period = period_s
+        self.ok = False
+        try:
+            import pynvml
+            pynvml.nvmlInit()
+            self.nv = pynvml
+            self.h = pynvml.nvmlDeviceGetHandleByIndex(device_index)
+            self.max_mhz = pynvml.nvmlDeviceGetMaxClockInfo(self.h, pynvml.NVML_CLOCK_SM)
+            self.ok = True
+        except Exception:
+            self.max_mhz = None
+        self._stop = threading.Event()
+
+    def _run(self):
+        nv = self.nv
+        while not self._stop.is_set():
+            try:
+                mhz = nv.nvmlDeviceGetClockInfo(self.h, nv.NVML_CLOCK_SM)
+                reasons = nv.nvmlDeviceGetCurrentClocksEventReasons(self.h)
+                self.samples.append((mhz, reasons))
+            except Exception:
+                pass
+            time.sleep(self.period)
+
+    def __enter__(self):
+        if self.ok:
+            self.t = threading.Thread(target=self._run, daemon=True)
+            self.t.start()
+        return self
+
+    def __exit__(self, *exc):
+        if self.ok:
+            self._stop.set()
+            self.t.join()
+
+    def summary(self):
+        if not self.ok:
+            return None
+        nv = self.nv
+        names = {
+            "gpu_idle": getattr(nv, "nvmlClocksEventReasonGpuIdle", 0x1),
+            "applications_clocks_setting": getattr(nv, "nvmlClocksEventReasonApplicationsClocksSetting", 0x2),
+            "sw_power_cap": getattr(nv, "nvmlClocksEventReasonSwPowerCap", 0x4),
+            "hw_slowdown": getattr(nv, "nvmlClocksEventReasonHwSlowdown", 0x8),
+            "sync_boost": getattr(nv, "nvmlClocksEventReasonSyncBoost", 0x10),
+            "sw_thermal_slowdown": getattr(nv, "nvmlClocksEventReasonSwThermalSlowdown", 0x20),
+            "hw_thermal_slowdown": getattr(nv, "nvmlClocksEventReasonHwThermalSlowdown", 0x40),
+            "hw_power_brake_slowdown": getattr(nv, "nvmlClocksEventReasonHwPowerBrakeSlowdown", 0x80),
+        }
+        seen = set()
+        for _, r in self.samples:
+            for k, bit in names.items():
+                if r & bit:
+                    seen.add(k)
+        mhz = [m for m, _ in self.samples]
+        return {"sm_mhz": statistics.median(mhz) if mhz else None, "sm_max_mhz": self.max_mhz,
+                "samples": len(mhz), "reasons": sorted(seen), "source": "nvml"}
+
+
+# ------------------------------------------------------------ our GPU arm
+def run_ours(args, rank, world):
+    import numpy as np
+    import torch
+
+    import fp8_fine_grained_19_b300 as fp8
+    import synth
+
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    lib = fp8.load()
+    stream = torch.cuda.current_stream()
+    sp = stream.cuda_stream
+
+    case = synth.dense_case("fprop")
+    x_h = case.x().pin_memory()
+    w_h = case.w().pin_memory()
+    x = x_h.to(dev)
+    w = w_h.to(dev)
+    qa = torch.empty((M, K), dtype=torch.uint8, device=dev)
+    sa = torch.empty((M, K // 128), dtype=torch.float32, device=dev)
+    qb = torch.empty((N, K), dtype=torch.uint8, device=dev)
+    sb = torch.empty((N // 128, K // 128), dtype=torch.float32, device=dev)
+    c = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+
+    def check(rc, what):
+        if rc != 0:
+            raise RuntimeError(f"{what}: {fp8.status_string(rc)}")
+
+    def act(xx):
+        check(lib.fp8_act_quant(xx.data_ptr(), fp8.BF16, M, K, qa.data_ptr(), sa.data_ptr(), 0, sp),
+              "act_quant")
+
+    def wq(ww):
+        check(lib.fp8_weight_quant(ww.data_ptr(), fp8.BF16, N, K, qb.data_ptr(), sb.data_ptr(),
+                                   None, None, 0, sp), "weight_quant")
+
+    def mm():
+        check(lib.fp8_blockscaled_gemm(qa.data_ptr(), sa.data_ptr(), qb.data_ptr(), sb.data_ptr(),
+                                       c.data_ptr(), fp8.BF16, M, N, K, 0, sp), "gemm")
+
+    def step(ev=None):
+        if ev is None:
+            act(x); wq(w); mm()
+            return
+        ev[0].record(stream); act(x); ev[1].record(stream); wq(w); ev[2].record(stream)
+        mm(); ev[3].record(stream)
+
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize()
+    if fp8.device_status() != fp8.OK:
+        raise RuntimeError("device status not OK after warm-up")
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(dev.index) as clk:
+        t0.record(stream)
+        for i in range(args.steps):
+            step(evs[i])
+        t1.record(stream)
+        torch.cuda.synchronize()
+    barrier()
+    ms = t0.elapsed_time(t1)
+    if world > 1:
+        tt = torch.tensor([ms], device=dev, dtype=torch.float64)
+        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+        ms = float(tt.item())
+    status = fp8.device_status()
+    if status != fp8.OK:
+        raise RuntimeError(f"device status {fp8.status_string(status)}")
+    t_act = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
+    t_wq = statistics.mean(e[1].elapsed_time(e[2]) for e in evs)
+    t_mm = statistics.mean(e[2].elapsed_time(e[3]) for e in evs)
+
+    # end to end through the public API: pinned host inputs in, result out, every step
+    e2e = None
+    if not args.no_e2e:
+        c_h = torch.empty((M, N), dtype=torch.bfloat16).pin_memory()
+        n2 = max(3, min(args.e2e_steps, args.steps))
+
+        def e2e_step():
+            x.copy_(x_h, non_blocking=True)
+            w.copy_(w_h, non_blocking=True)
+            step()
+            c_h.copy_(c, non_blocking=True)
+
+        e2e_step()
+        torch.cuda.synchronize()
+        barrier()
+        a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a0.record(stream)
+        for _ in range(n2):
+            e2e_step()
+        a1.record(stream)
+        torch.cuda.synchronize()
+        barrier()
+        ms2 = a0.elapsed_time(a1)
+        if world > 1:
+            tt = torch.tensor([ms2], device=dev, dtype=torch.float64)
+            torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+            ms2 = float(tt.item())
+        e2e = {"value": round(world * n2 * FLOPS / (ms2 * 1e-3) / 1e12, 3), "unit": "TFLOP/s",
+               "steps": n2,
+               "h2d_bytes_per_step": x_h.numel() * 2 + w_h.numel() * 2,
+               "d2h_bytes_per_step": c_h.numel() * 2}
+
+    pk = peaks()
+    fp8_peak = 2.0 * pk["bf16"]
+    gemm_tflops = FLOPS / (t_mm * 1e-3) / 1e12
+    aq_bytes = M * K * 2 + M * K + M * (K // 128) * 4
+    wq_bytes = N * K * 2 + N * K + (N // 128) * (K // 128) * 4
+    gemm_bytes = M * K + N * K + (M + N // 128) * (K // 128) * 4 + M * N * 2
+    aq_gbs = aq_bytes / (t_act * 1e-3) / 1e9
+    wq_gbs = wq_bytes / (t_wq * 1e-3) / 1e9
+    out = {
+        "metric": METRIC,
+        "value": round(world * args.steps * FLOPS / (ms * 1e-3) / 1e12, 3),
+        "unit": "TFLOP/s",
+        "n_gpus": world, "steps": args.steps, "warmup": max(args.warmup, 3),
+        "ms_per_step": round(ms / args.steps, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "e4m3 x e4m3 -> f32 accumulate, bf16 out",
+        "data": "synthetic (seeded N(0,1) X with 0.1% x100 outliers, N(0,0.02) W)",
+        "config": {"workload": WORKLOAD, "M": M, "N": N, "K": K,
+                   "step": "act_quant(X) + weight_quant(W) + gemm -> bf16",
+                   "l2": "per-step working set 0.66 GB > 126 MB L2 (inputs larger than L2)",
+                   "parallelism": f"{world} independent replica(s)"},
+        "roofline": {"kernel": "blockscaled_gemm", "bound": "tensor",
+                     "achieved": round(gemm_tflops, 2),
+                     "peak": round(fp8_peak, 1), "unit": "TFLOP/s",
+                     "frac": round(gemm_tflops / fp8_peak, 4),
+                     "peak_source": f"2 x bf16 burst of {pk['source']} ({pk['bf16']} TF/s)",
+                     "frac_of_nominal_4500": round(gemm_tflops / 4500.0, 4),
+                     "traffic": traffic_for_current_kernel(),
+                     "algorithmic_bytes": gemm_bytes},
+        "per_op": {
+            "act_quant": {"ms": round(t_act, 5), "GB/s": round(aq_gbs, 1),
+                          "frac_hbm": round(aq_gbs / pk["hbm_gbs"], 4), "bytes": aq_bytes},
+            "weight_quant": {"ms": round(t_wq, 5), "GB/s": round(wq_gbs, 1),
+                             "frac_hbm": round(wq_gbs / pk["hbm_gbs"], 4), "bytes": wq_bytes},
+            "gemm": {"ms": round(t_mm, 5), "TFLOP/s": round(gemm_tflops, 2),
+                     "frac_fp8_peak": round(gemm_tflops / fp8_peak, 4)},
+            "hbm_peak_gbs": pk["hbm_gbs"], "hbm_peak_source": pk["source"],
+        },
+        "e2e": e2e,
+        "gpu_launches": 3 * args.steps,
+        "clocks": clk.summary(),
+    }
+    return out
+
+
+# ------------------------------------------------------------- CPU oracle
+def oracle_sample(rows_aq=2048, rows_wq=2048, rows_g=512, cols_g=4096, seed=0):
+    """Time the oracle on a bounded sample of one step; extrapolate to the full step.
+
+    Returns (seconds for the full step, description, threads)."""
+    import numpy as np
+
+    import oracle
+    import synth
+
+    case = synth.dense_case("fprop")
+    x = synth.normal_f32((rows_aq, K), 1.0, seed, synth.TAG_X, **case.x_outlier)
+    w = synth.normal_f32((rows_wq, K), 0.02, seed, synth.TAG_W)
+    t0 = time.perf_counter()
+    qa, sa = oracle.act_quant(x)
+    t1 = time.perf_counter()
+    qb, sb = oracle.weight_quant(w)
+    t2 = time.perf_counter()
+    reps = -(-cols_g // rows_wq)
+    qbg = np.concatenate([qb] * reps)[:cols_g]
+    sbg = np.concatenate([sb] * reps)[: cols_g // 128]
+    oracle.gemm(qa[:rows_g], sa[:rows_g], qbg, sbg)
+    t3 = time.perf_counter()
+    full = (t1 - t0) * (M / rows_aq) + (t2 - t1) * (N / rows_wq) + \
+        (t3 - t2) * (M * N) / (rows_g * cols_g)
+    desc = (f"act_quant {rows_aq}x{K}, weight_quant {rows_wq}x{K}, gemm {rows_g}x{cols_g}x{K}; "
+            f"extrapolated to {M}x{N}x{K} by rows/columns (sample {t3 - t0:.1f} s)")
+    return full, desc, t3 - t0
+
+
+def cpu_threads():
+    try:
+        from threadpoolctl import threadpool_info
+        n = max((i.get("num_threads", 1) for i in threadpool_info()), default=1)
+        return int(n)
+    except Exception:
+        return len(os.sched_getaffinity(0))
+
+
+def run_reference(args):
+    # size each step's sample so that warm-up + steps stay within about two minutes
+    budget = 120.0
+    n = max(args.steps, 1) + max(args.warmup, 0)
+    scale = 1.0
+    full, _, secs = oracle_sample(256, 256, 64, 1024)
+    per = secs
+    while per * n < budget * 0.5 and scale < 64:
+        scale *= 2
+        per = secs * scale
+    while per * n > budget and scale > 1 / 64:
+        scale /= 2
+        per = secs * scale
+    ra = max(16, int(256 * scale))
+    rw = max(128, int(256 * scale) // 128 * 128)
+    rg = max(8, int(64 * scale))
+    for _ in range(max(args.warmup, 0)):
+        oracle_sample(ra, rw, rg, 1024)
+    fulls = []
+    t0 = time.perf_counter()
+    desc = ""
+    for _ in range(max(args.steps, 1)):
+        f, desc, _ = oracle_sample(ra, rw, rg, 1024)
+        fulls.append(f)
+    wall = time.perf_counter() - t0
+    t_full = statistics.mean(fulls)
+    val = FLOPS / t_full / 1e12
+    cores = cpu_threads()
+    return {
+        "metric": METRIC, "impl": "reference", "value": round(val, 6), "unit": "TFLOP/s",
+        "n_gpus": args.gpus, "steps": max(args.steps, 1), "warmup": max(args.warmup, 0),
+        "ms_per_step": round(t_full * 1e3, 3), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64 (oracle)", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "M": M, "N": N, "K": K},
+        "cpu_baseline": {"value": round(val, 6), "unit": "TFLOP/s", "cores": cores,
+                         "kind": "oracle", "sample": desc, "wall_s": round(wall, 2)},
+        "e2e": {"value": round(val, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    args = parse()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args)), flush=True)
+        return
+    if world > 1:
+        import torch
+        torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
+        torch.distributed.init_process_group("nccl")
+    out = run_ours(args, rank, world)
+    if rank == 0:
+        if not args.no_cpu_baseline:
+            full, desc, _ = oracle_sample()
+            out["cpu_baseline"] = {"value": round(FLOPS / full / 1e12, 6), "unit": "TFLOP/s",
+                                   "cores": cpu_threads(), "kind": "oracle", "sample": desc}
+        print(json.dumps(out), flush=True)
+    if world > 1:
+        import torch
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,206 @@
+"""Python binding of libfp8fg.so (fine-grained FP8 quantisation and block-scaled GEMMs).
+
+Argument marshalling only: every step runs in the library's CUDA kernels.
+PyTorch supplies device memory and the current stream.  The functions have the
+C ABI's names without the ``fp8_`` prefix; each checks tensor dtypes, devices
+and contiguity, allocates the outputs with torch, and raises ``Fp8Error`` on a
+non-OK status.  There is no CPU fallback: without the built library or a CUDA
+device the calls raise.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+__all__ = [
+    "Fp8Error", "load", "lib_path", "act_quant", "weight_quant", "gemm", "grouped_gemm",
+    "device_status", "set_wait_limit", "selftest_wait_timeout", "status_string",
+    "OK", "ERR_INVALID_ARG", "ERR_UNSUPPORTED_SHAPE", "ERR_MISALIGNED", "ERR_CUDA",
+    "ERR_TIMEOUT", "ERR_BAD_OFFSETS", "POW2", "TRANSPOSE", "B_TILE1x128", "BF16", "F32",
+]
+
+OK, ERR_INVALID_ARG, ERR_UNSUPPORTED_SHAPE, ERR_MISALIGNED, ERR_CUDA, ERR_TIMEOUT, \
+    ERR_BAD_OFFSETS = range(7)
+BF16, F32 = 0, 1
+POW2, TRANSPOSE, B_TILE1x128 = 1, 2, 4
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_LIB: ctypes.CDLL | None = None
+
+_vp, _i64, _u32, _i32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_uint, ctypes.c_int32
+_SIGS = {
+    "fp8_act_quant": [_vp, ctypes.c_int, _i64, _i64, _vp, _vp, _u32, _vp],
+    "fp8_weight_quant": [_vp, ctypes.c_int, _i64, _i64, _vp, _vp, _vp, _vp, _u32, _vp],
+    "fp8_blockscaled_gemm": [_vp, _vp, _vp, _vp, _vp, ctypes.c_int, _i64, _i64, _i64, _u32, _vp],
+    "fp8_grouped_gemm": [_vp, _vp, _vp, _i32, _i64, _vp, _vp, _vp, ctypes.c_int, _i64, _i64,
+                         _u32, _vp],
+    "fp8_get_device_status": [_vp],
+    "fp8fg_status_string": [ctypes.c_int],
+    "fp8fg_abi_version": [],
+    "fp8fg_set_wait_limit": [ctypes.c_uint64],
+    "fp8fg_selftest_wait_timeout": [ctypes.c_uint32, _vp],
+}
+
+
+class Fp8Error(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {status_string(status)} (status {status})")
+
+
+def lib_path() -> str:
+    return os.path.join(_HERE, "libfp8fg.so")
+
+
+def load() -> ctypes.CDLL:
+    """Load libfp8fg.so from this package directory (raises if it is missing)."""
+    global _LIB
+    if _LIB is not None:
+        return _LIB
+    path = lib_path()
+    if not os.path.exists(path):
+        raise RuntimeError(f"{path} is missing: build it with "
+                           "`python -m fp8_fine_grained_19_b300.build`")
+    lib = ctypes.CDLL(path)
+    for name, args in _SIGS.items():
+        f = getattr(lib, name)
+        f.argtypes = args
+        f.restype = ctypes.c_char_p if name == "fp8fg_status_string" else (
+            None if name == "fp8fg_set_wait_limit" else ctypes.c_int)
+    _LIB = lib
+    return lib
+
+
+def status_string(status: int) -> str:
+    return load().fp8fg_status_string(int(status)).decode()
+
+
+def _check(status: int, where: str) -> None:
+    if status != OK:
+        raise Fp8Error(status, where)
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return int(stream.cuda_stream)
+
+
+def _ptr(t: torch.Tensor | None) -> int | None:
+    return None if t is None else t.data_ptr()
+
+
+def _need(t: torch.Tensor, dtypes, name: str) -> None:
+    if not isinstance(t, torch.Tensor) or t.device.type != "cuda":
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype not in dtypes:
+        raise ValueError(f"{name} has dtype {t.dtype}, expected one of {dtypes}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def _src_dtype(t: torch.Tensor) -> int:
+    return BF16 if t.dtype == torch.bfloat16 else F32
+
+
+_SRC = (torch.bfloat16, torch.float32)
+
+
+def act_quant(x: torch.Tensor, pow2: bool = False, transpose: bool = False, stream=None):
+    """1x128 tiles -> (q uint8 [M, K], s float32 [M, K/128]);
+    transpose=True: 128x1 tiles -> (q [K, M], s [K, M/128])."""
+    _need(x, _SRC, "x")
+    M, K = x.shape
+    if transpose:
+        q = torch.empty((K, M), dtype=torch.uint8, device=x.device)
+        s = torch.empty((K, M // 128 if M % 128 == 0 else 1), dtype=torch.float32, device=x.device)
+    else:
+        q = torch.empty((M, K), dtype=torch.uint8, device=x.device)
+        s = torch.empty((M, K // 128 if K % 128 == 0 else 1), dtype=torch.float32, device=x.device)
+    flags = (POW2 if pow2 else 0) | (TRANSPOSE if transpose else 0)
+    _check(load().fp8_act_quant(_ptr(x), _src_dtype(x), M, K, _ptr(q), _ptr(s), flags,
+                                _stream(stream)), "fp8_act_quant")
+    return q, s
+
+
+def weight_quant(w: torch.Tensor, pow2: bool = False, transposed: bool = False, stream=None):
+    """128x128 blocks -> (q [N, K], s [N/128, K/128]) (+ (q_t [K, N], s_t) if transposed)."""
+    _need(w, _SRC, "w")
+    N, K = w.shape
+    q = torch.empty((N, K), dtype=torch.uint8, device=w.device)
+    s = torch.empty((max(N // 128, 1), max(K // 128, 1)), dtype=torch.float32, device=w.device)
+    qt = st = None
+    if transposed:
+        qt = torch.empty((K, N), dtype=torch.uint8, device=w.device)
+        st = torch.empty((max(K // 128, 1), max(N // 128, 1)), dtype=torch.float32, device=w.device)
+    _check(load().fp8_weight_quant(_ptr(w), _src_dtype(w), N, K, _ptr(q), _ptr(s), _ptr(qt),
+                                   _ptr(st), POW2 if pow2 else 0, _stream(stream)),
+           "fp8_weight_quant")
+    return (q, s, qt, st) if transposed else (q, s)
+
+
+def _out_code(dtype) -> int:
+    if dtype == torch.bfloat16:
+        return BF16
+    if dtype == torch.float32:
+        return F32
+    raise ValueError(f"unsupported output dtype {dtype}")
+
+
+def gemm(a, sa, b, sb, out_dtype=torch.bfloat16, b_tile: bool = False, out=None, stream=None):
+    """C[M, N] = sum_kb (A_kb . B_kb^T) * sa[:, kb] * sb(., kb), promoted to FP32 per 128 K."""
+    for t, n in ((a, "a"), (b, "b")):
+        _need(t, (torch.uint8,), n)
+    for t, n in ((sa, "sa"), (sb, "sb")):
+        _need(t, (torch.float32,), n)
+    M, K = a.shape
+    N = b.shape[0]
+    if b.shape[1] != K:
+        raise ValueError("a and b disagree on K")
+    if out is None:
+        out = torch.empty((M, N), dtype=out_dtype, device=a.device)
+    _need(out, (torch.bfloat16, torch.float32), "out")
+    _check(load().fp8_blockscaled_gemm(_ptr(a), _ptr(sa), _ptr(b), _ptr(sb), _ptr(out),
+                                       _out_code(out.dtype), M, N, K,
+                                       B_TILE1x128 if b_tile else 0, _stream(stream)),
+           "fp8_blockscaled_gemm")
+    return out
+
+
+def grouped_gemm(a, sa, offsets, b, sb, out_dtype=torch.bfloat16, out=None, stream=None):
+    """Per-expert gemm over row groups offsets[e]..offsets[e+1] (device int32 [E+1])."""
+    _need(a, (torch.uint8,), "a")
+    _need(b, (torch.uint8,), "b")
+    _need(sa, (torch.float32,), "sa")
+    _need(sb, (torch.float32,), "sb")
+    _need(offsets, (torch.int32,), "offsets")
+    T, K = a.shape
+    E, N, Kb = b.shape
+    if Kb != K or offsets.numel() != E + 1:
+        raise ValueError("shape mismatch between a, b and offsets")
+    if out is None:
+        out = torch.empty((T, N), dtype=out_dtype, device=a.device)
+    _need(out, (torch.bfloat16, torch.float32), "out")
+    _check(load().fp8_grouped_gemm(_ptr(a), _ptr(sa), _ptr(offsets), E, T, _ptr(b), _ptr(sb),
+                                   _ptr(out), _out_code(out.dtype), N, K, 0, _stream(stream)),
+           "fp8_grouped_gemm")
+    return out
+
+
+def device_status(stream=None) -> int:
+    """Synchronise the stream; return and clear the library's device status word."""
+    return int(load().fp8_get_device_status(_stream(stream)))
+
+
+def set_wait_limit(cycles: int) -> None:
+    load().fp8fg_set_wait_limit(int(cycles))
+
+
+def selftest_wait_timeout(limit_cycles: int = 1 << 20, stream=None) -> int:
+    """Run the bounded-wait self-test; returns the device status it produced."""
+    _check(load().fp8fg_selftest_wait_timeout(int(limit_cycles), _stream(stream)),
+           "fp8fg_selftest_wait_timeout")
+    return device_status(stream)

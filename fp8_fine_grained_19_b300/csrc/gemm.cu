@@ -1,0 +1,522 @@
+// Block-scaled FP8 GEMM with per-128-K promotion into FP32 (sm_103a).
+//
+// Method (page 2, inprokorea.com free #735329): the tensor cores accumulate
+// only within one K group; after each group of 128 the partial result is moved
+// to FP32 registers on the CUDA cores, multiplied by the group's activation
+// tile scale and weight block scale, and added to a full-precision FP32
+// accumulator (promotion passage, Figure 6; per-group-scaling passage).  The
+// pages describe this on H800 with two warpgroups alternating WGMMA and
+// promotion (page 1, passage on two concurrent WGMMAs); that is prior art.
+//
+// B300 design (one persistent CTA per SM, 384 threads, 1 CTA/SM):
+//   warp 8      TMA producer: one 128x128 A tile + one 256x128 B tile of E4M3
+//               codes per 128-K slice into a 4-stage ring (128-byte swizzle).
+//   warp 9      MMA issuer: one thread issues 4 x tcgen05.mma (M128 N256 K32,
+//               kind::f8f6f4, FP32 accumulate) per slice into one of two TMEM
+//               buffers (2 x 256 columns), then commits to the stage's "empty"
+//               barrier and the buffer's "full" barrier.
+//   warps 0-7   promotion/epilogue: warp w reads TMEM lanes 32(w%4).. (its 32
+//               rows) and columns 128(w/4).. (its half of N) of the finished
+//               buffer with tcgen05.ld, frees the buffer, and does
+//               acc += P * (sa[row,kb] * sb[.,kb]) with packed f32x2 FMAs.
+//               The FP32 accumulator (128 values per thread) stays in
+//               registers for the whole tile; TMEM only ever holds one
+//               slice's partial, so the MMA of slice kb+1 overlaps the
+//               promotion of slice kb, and the next tile's MMAs overlap this
+//               tile's final store.
+// Tiles are visited in groups of 16 M-tiles (all N-tiles of a group before the
+// next), so a group's A rows stay in L2 while B streams once per group.
+// Every pipeline wait is bounded (FP8FG_ERR_TIMEOUT, see device_common.cuh).
+
+#include <cuda_bf16.h>
+
+#include "device_common.cuh"
+#include "launch.h"
+
+namespace fp8fg {
+
+namespace {
+
+constexpr int BM = 128, BN = 256, BK = 128;
+constexpr int STAGES = 4;
+constexpr int A_BYTES = BM * BK;
+constexpr int B_BYTES = BN * BK;
+constexpr int NUM_EPI_WARPS = 8;
+constexpr int PRODUCER_WARP = 8;
+constexpr int MMA_WARP = 9;
+constexpr int NUM_THREADS = 384;      // 3 warpgroups: 2 promotion/epilogue, 1 TMA+MMA
+// Register split (per thread): launched at 168 (= 65536 / 384 rounded down to 8);
+// the TMA/MMA warpgroup gives up to 56 and the two promotion warpgroups take 224:
+// 2 x 224 + 56 = 3 x 168, so the re-allocation never waits on registers.
+constexpr int REGS_LAUNCH = 168;
+constexpr int REGS_PRODUCER = 56;
+constexpr int REGS_EPILOGUE = 224;
+static_assert(2 * REGS_EPILOGUE + REGS_PRODUCER <= 3 * REGS_LAUNCH, "register split");
+constexpr int TMEM_COLS = 512;
+constexpr int GROUP_M = 16;
+constexpr int MAX_EXPERTS = 1024;
+constexpr uint32_t IDESC = idesc_e4m3_f32(BM, BN);
+
+struct GemmParams {
+  const float* sa;        // [rows, nkb]
+  const float* sb;        // block: [E][N/128][nkb]; tile: [N][nkb]
+  void* c;                // [rows, N]
+  const int32_t* offsets; // grouped only, [E+1]
+  int M;                  // dense: rows of A/C; grouped: total rows
+  int N, K, nkb;
+  int m_tiles, n_tiles;   // dense tiling (m_tiles unused when grouped)
+  int E;
+  int c_f32;
+  int b_tile;
+  long long wait_limit;
+  int* status;            // library status word
+};
+
+struct Smem {
+  uint8_t a[STAGES][A_BYTES];     // 1024-byte aligned (offset 0)
+  uint8_t b[STAGES][B_BYTES];
+  uint64_t full_bar[STAGES];
+  uint64_t empty_bar[STAGES];
+  uint64_t tfull_bar[2];
+  uint64_t tempty_bar[2];
+  uint64_t drain_bar;
+  uint32_t tmem_base;
+  int abort_flag;
+  int bad_offsets;
+  int num_tiles;
+  float sbt[2][2][128];           // tile-mode B scales: [column half][slice counter parity][col]
+  int cum[MAX_EXPERTS + 1];       // grouped: tile prefix per expert
+  int row0[MAX_EXPERTS + 1];      // grouped: copy of offsets
+};
+
+struct Tile {
+  int m0;       // first row of A / C
+  int row_end;  // rows >= row_end are not stored (expert end or M)
+  int n0;       // first column
+  int e;        // expert (0 when dense)
+};
+
+template <bool GROUPED>
+__device__ __forceinline__ Tile tile_of(int t, const GemmParams& p, const Smem& sm) {
+  Tile r;
+  if constexpr (!GROUPED) {
+    const int group = GROUP_M * p.n_tiles;
+    const int g = t / group;
+    const int first = g * GROUP_M;
+    const int gm = min(GROUP_M, p.m_tiles - first);
+    const int local = t - g * group;
+    const int mb = first + local % gm;
+    const int nb = local / gm;
+    r.m0 = mb * BM;
+    r.row_end = p.M;
+    r.n0 = nb * BN;
+    r.e = 0;
+  } else {
+    // largest e with cum[e] <= t (experts with no tiles have cum[e] == cum[e+1])
+    int lo = 0, hi = p.E - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (sm.cum[mid] <= t) lo = mid; else hi = mid - 1;
+    }
+    const int e = lo;
+    const int rows = sm.row0[e + 1] - sm.row0[e];
+    const int mt = (rows + BM - 1) / BM;
+    const int local = t - sm.cum[e];
+    const int nb = local / mt;
+    const int mb = local - nb * mt;
+    r.m0 = sm.row0[e] + mb * BM;
+    r.row_end = sm.row0[e + 1];
+    r.n0 = nb * BN;
+    r.e = e;
+  }
+  return r;
+}
+
+template <bool GROUPED>
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    blockscaled_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
+                            const __grid_constant__ CUtensorMap tmB, const GemmParams p) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  // 1024-byte alignment of the operand stages (required by the 128B swizzle)
+  Smem& sm = *reinterpret_cast<Smem*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  volatile int* abort_flag = &sm.abort_flag;
+
+  // ---------------------------------------------------------------- set-up
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(smem_u32(&sm.full_bar[s]), 1);
+      mbar_init(smem_u32(&sm.empty_bar[s]), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(smem_u32(&sm.tfull_bar[b]), 1);
+      mbar_init(smem_u32(&sm.tempty_bar[b]), NUM_EPI_WARPS);
+    }
+    mbar_init(smem_u32(&sm.drain_bar), 1);
+    fence_mbar_init();
+    sm.abort_flag = 0;
+    sm.bad_offsets = 0;
+  }
+  if (warp == PRODUCER_WARP && lane == 0) {
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+  }
+  if constexpr (GROUPED) {
+    // Copy and check the offsets, then prefix the per-expert tile counts with
+    // one warp: lane l owns a contiguous chunk of experts.
+    if (warp == 0) {
+      const int E = p.E;
+      const int per = (E + 31) / 32;
+      const int e0 = min(E, lane * per), e1 = min(E, e0 + per);
+      int bad = 0, local = 0;
+      for (int e = e0; e < e1; ++e) {
+        const int r0 = p.offsets[e], r1 = p.offsets[e + 1];
+        sm.row0[e] = r0;
+        if (r1 < r0 || r0 < 0 || r1 > p.M) bad = 1;
+        local += ((r1 - r0) + BM - 1) / BM * p.n_tiles;
+      }
+      int incl = local;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const int v = __shfl_up_sync(0xFFFFFFFFu, incl, off);
+        if (lane >= off) incl += v;
+      }
+      int run = incl - local;
+      for (int e = e0; e < e1; ++e) {
+        sm.cum[e] = run;
+        const int r0 = p.offsets[e], r1 = p.offsets[e + 1];
+        run += max(0, (r1 - r0) + BM - 1) / BM * p.n_tiles;
+      }
+      bad = __any_sync(0xFFFFFFFFu, bad);
+      if (lane == 31) sm.num_tiles = incl;
+      if (lane == 0) {
+        sm.row0[E] = p.offsets[E];
+        if (p.offsets[0] != 0 || p.offsets[E] != p.M) bad = 1;
+        sm.cum[E] = 0;
+        sm.bad_offsets = bad;
+      }
+    }
+  } else {
+    if (threadIdx.x == 0) sm.num_tiles = p.m_tiles * p.n_tiles;
+  }
+  if (warp == MMA_WARP) {
+    tmem_alloc(smem_u32(&sm.tmem_base), TMEM_COLS);
+    tmem_relinquish();
+    tc_fence_before();
+  }
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = sm.tmem_base;
+  const bool bad = GROUPED && sm.bad_offsets;
+  if (bad && threadIdx.x == 0) record_status(p.status, FP8FG_ERR_BAD_OFFSETS);
+  const int num_tiles = bad ? 0 : sm.num_tiles;
+  const int nkb = p.nkb;
+
+  if (warp >= NUM_EPI_WARPS) {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(REGS_PRODUCER));
+    if (warp == PRODUCER_WARP) {
+    // --------------------------------------------------------- TMA producer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t issued = 0, issued_parity = 0;   // per-stage bits
+      for (int t = blockIdx.x; t < num_tiles && !*abort_flag; t += gridDim.x) {
+        const Tile tl = tile_of<GROUPED>(t, p, sm);
+        for (int kb = 0; kb < nkb; ++kb) {
+          if (!mbar_wait(smem_u32(&sm.empty_bar[stage]), phase ^ 1, p.wait_limit, abort_flag, p.status))
+            break;
+          const uint32_t fb = smem_u32(&sm.full_bar[stage]);
+          mbar_arrive_expect_tx(fb, A_BYTES + B_BYTES);
+          tma_load_2d(smem_u32(sm.a[stage]), &tmA, fb, kb * BK, tl.m0);
+          if constexpr (GROUPED)
+            tma_load_3d(smem_u32(sm.b[stage]), &tmB, fb, kb * BK, tl.n0, tl.e);
+          else
+            tma_load_2d(smem_u32(sm.b[stage]), &tmB, fb, kb * BK, tl.n0);
+          issued |= 1u << stage;
+          issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
+          if (++stage == STAGES) { stage = 0; phase ^= 1; }
+        }
+      }
+      // never leave the CTA with a bulk copy still landing in shared memory
+      volatile int never = 0;
+      for (int s = 0; s < STAGES; ++s)
+        if (issued & (1u << s))
+          mbar_wait(smem_u32(&sm.full_bar[s]), (issued_parity >> s) & 1, p.wait_limit, &never, p.status);
+    }
+  } else if (warp == MMA_WARP) {
+    // ----------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t it = 0;                              // slice counter (TMEM buffers)
+      bool ok = true;
+      for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+        for (int kb = 0; kb < nkb; ++kb, ++it) {
+          const uint32_t buf = it & 1, bpar = (it >> 1) & 1;
+          if (!mbar_wait(smem_u32(&sm.tempty_bar[buf]), bpar ^ 1, p.wait_limit, abort_flag, p.status) ||
+              !mbar_wait(smem_u32(&sm.full_bar[stage]), phase, p.wait_limit, abort_flag, p.status)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a0 = smem_u32(sm.a[stage]);
+          const uint32_t b0 = smem_u32(sm.b[stage]);
+          const uint32_t d = tmem_base + buf * BN;
+#pragma unroll
+          for (int k = 0; k < BK / 32; ++k)
+            mma_f8(d, smem_desc_sw128(a0 + 32 * k), smem_desc_sw128(b0 + 32 * k), IDESC,
+                   k > 0 ? 1u : 0u);
+          mma_commit(smem_u32(&sm.empty_bar[stage]));
+          mma_commit(smem_u32(&sm.tfull_bar[buf]));
+          if (++stage == STAGES) { stage = 0; phase ^= 1; }
+        }
+      }
+      // all issued MMAs must finish before TMEM is released
+      mma_commit(smem_u32(&sm.drain_bar));
+      volatile int never = 0;
+      mbar_wait(smem_u32(&sm.drain_bar), 0, p.wait_limit, &never, p.status);
+    }
+    }
+  } else {
+    // ------------------------------------------------ promotion + epilogue
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(REGS_EPILOGUE));
+    const int quad = warp & 3;                      // TMEM lane quadrant
+    const int half = warp >> 2;                     // N half of the tile
+    const int tid_h = threadIdx.x & 127;            // index within the half's warpgroup
+    const int n_blocks = p.N / 128;                 // block-mode scale rows per expert
+    uint32_t it = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+      const Tile tl = tile_of<GROUPED>(t, p, sm);
+      const int row = tl.m0 + quad * 32 + lane;
+      const bool row_ok = row < tl.row_end;
+      const int col_h = tl.n0 + half * 128;         // first column of this half
+      const bool half_ok = col_h < p.N;
+      const float* sa_row = p.sa + static_cast<int64_t>(row_ok ? row : 0) * nkb;
+      const float* sb_ptr;
+      if (p.b_tile) {
+        const int col = col_h + tid_h;
+        sb_ptr = p.sb + static_cast<int64_t>(col < p.N ? col : 0) * nkb;
+      } else {
+        sb_ptr = p.sb + (static_cast<int64_t>(tl.e) * n_blocks + (half_ok ? col_h / 128 : 0)) * nkb;
+      }
+      const bool sb_ok = p.b_tile ? (col_h + tid_h < p.N) : half_ok;
+
+      uint64_t acc[64];
+#pragma unroll
+      for (int j = 0; j < 64; ++j) acc[j] = 0;
+
+      float sa_next = row_ok ? __ldg(sa_row) : 0.0f;
+      float sb_next = sb_ok ? __ldg(sb_ptr) : 0.0f;
+      for (int kb = 0; kb < nkb; ++kb, ++it) {
+        const float sa_cur = sa_next, sb_cur = sb_next;
+        if (kb + 1 < nkb) {
+          sa_next = row_ok ? __ldg(sa_row + kb + 1) : 0.0f;
+          sb_next = sb_ok ? __ldg(sb_ptr + kb + 1) : 0.0f;
+        }
+        const uint32_t buf = it & 1, bpar = (it >> 1) & 1;
+        const bool got =
+            mbar_wait(smem_u32(&sm.tfull_bar[buf]), bpar, p.wait_limit, abort_flag, p.status);
+        if (p.b_tile) {
+          // publish this slice's column scales to the half; the barrier also
+          // takes a vote so that all 128 threads leave together on an abort
+          sm.sbt[half][it & 1][tid_h] = sb_cur;
+          if (bar_any(1 + half, 128, !got)) {
+            ok = false;
+            break;
+          }
+        } else if (!got) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + buf * BN +
+                               half * 128;
+        if (!p.b_tile) {
+          const float s = sa_cur * sb_cur;
+          const uint64_t s2 = pack2(__float_as_uint(s), __float_as_uint(s));
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            uint32_t r[32];
+            tmem_ld_32cols(taddr + c * 32, r);
+            tmem_ld_wait();
+#pragma unroll
+            for (int j = 0; j < 16; ++j) fma2(acc[c * 16 + j], pack2(r[2 * j], r[2 * j + 1]), s2);
+          }
+        } else {
+          const uint64_t sa2 = pack2(__float_as_uint(sa_cur), __float_as_uint(sa_cur));
+          const float* sbv = sm.sbt[half][it & 1];
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            uint32_t r[32];
+            tmem_ld_32cols(taddr + c * 32, r);
+            tmem_ld_wait();
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              const float2 sbp = *reinterpret_cast<const float2*>(&sbv[c * 32 + 2 * j]);
+              const uint64_t coef =
+                  mul2(pack2(__float_as_uint(sbp.x), __float_as_uint(sbp.y)), sa2);
+              fma2(acc[c * 16 + j], pack2(r[2 * j], r[2 * j + 1]), coef);
+            }
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&sm.tempty_bar[buf]));
+      }
+      if (!ok) break;
+
+      // --- store this thread's row segment (128 columns of its half)
+      if (row_ok && half_ok) {
+        if (p.c_f32) {
+          float* dst = static_cast<float*>(p.c) + static_cast<int64_t>(row) * p.N + col_h;
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            if (col_h + 4 * j + 4 <= p.N) {
+              float x0, x1, x2, x3;
+              unpack2(acc[2 * j], x0, x1);
+              unpack2(acc[2 * j + 1], x2, x3);
+              *reinterpret_cast<float4*>(dst + 4 * j) = make_float4(x0, x1, x2, x3);
+            }
+          }
+        } else {
+          __nv_bfloat16* dst =
+              static_cast<__nv_bfloat16*>(p.c) + static_cast<int64_t>(row) * p.N + col_h;
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            if (col_h + 8 * j + 8 <= p.N) {
+              uint32_t w[4];
+#pragma unroll
+              for (int i = 0; i < 4; ++i) {
+                float lo, hi;
+                unpack2(acc[4 * j + i], lo, hi);
+                const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+                w[i] = *reinterpret_cast<const uint32_t*>(&v);
+              }
+              *reinterpret_cast<uint4*>(dst + 8 * j) = make_uint4(w[0], w[1], w[2], w[3]);
+            }
+          }
+        }
+      }
+    }
+  }
+
+  // -------------------------------------------------------------- teardown
+  __syncthreads();
+  if (warp == MMA_WARP) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, TMEM_COLS);
+  }
+}
+
+// One CTA waits on an mbarrier that nothing arrives on; the bounded wait must
+// give up, record FP8FG_ERR_TIMEOUT and return.
+__global__ void wait_timeout_selftest_kernel(long long limit, int* status) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&bar), 1);
+    fence_mbar_init();
+    abort_flag = 0;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) mbar_wait(smem_u32(&bar), 0, limit, &abort_flag, status);
+  __syncthreads();
+}
+
+constexpr size_t kSmemBytes = sizeof(Smem) + 1024;
+
+bool make_maps(CUtensorMap* mA, CUtensorMap* mB, const uint8_t* a, int64_t rowsA,
+               const uint8_t* b, int64_t E, int64_t N, int64_t K) {
+  const uint64_t dA[2] = {static_cast<uint64_t>(K), static_cast<uint64_t>(rowsA)};
+  const uint64_t sA[1] = {static_cast<uint64_t>(K)};
+  const uint32_t boxA[2] = {BK, BM};
+  if (!encode_tensor_map_u8(mA, a, 2, dA, sA, boxA)) return false;
+  if (E == 0) {
+    const uint64_t dB[2] = {static_cast<uint64_t>(K), static_cast<uint64_t>(N)};
+    const uint64_t sB[1] = {static_cast<uint64_t>(K)};
+    const uint32_t boxB[2] = {BK, BN};
+    return encode_tensor_map_u8(mB, b, 2, dB, sB, boxB);
+  }
+  const uint64_t dB[3] = {static_cast<uint64_t>(K), static_cast<uint64_t>(N),
+                          static_cast<uint64_t>(E)};
+  const uint64_t sB[2] = {static_cast<uint64_t>(K), static_cast<uint64_t>(N * K)};
+  const uint32_t boxB[3] = {BK, BN, 1};
+  return encode_tensor_map_u8(mB, b, 3, dB, sB, boxB);
+}
+
+template <bool GROUPED>
+cudaError_t set_smem_attr() {
+  static const cudaError_t e = cudaFuncSetAttribute(
+      blockscaled_gemm_kernel<GROUPED>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+      static_cast<int>(kSmemBytes));
+  return e;
+}
+
+}  // namespace
+
+fp8fg_status launch_gemm(const uint8_t* a, const float* sa, const uint8_t* b, const float* sb,
+                         void* c, fp8fg_dtype ct, int64_t M, int64_t N, int64_t K, bool b_tile,
+                         cudaStream_t st) {
+  CUtensorMap mA, mB;
+  if (!make_maps(&mA, &mB, a, M, b, 0, N, K)) return FP8FG_ERR_CUDA;
+  if (set_smem_attr<false>() != cudaSuccess) return FP8FG_ERR_CUDA;
+  GemmParams p{};
+  p.sa = sa;
+  p.sb = sb;
+  p.c = c;
+  p.offsets = nullptr;
+  p.M = static_cast<int>(M);
+  p.N = static_cast<int>(N);
+  p.K = static_cast<int>(K);
+  p.nkb = static_cast<int>(K / BK);
+  p.m_tiles = static_cast<int>((M + BM - 1) / BM);
+  p.n_tiles = static_cast<int>((N + BN - 1) / BN);
+  p.E = 1;
+  p.c_f32 = ct == FP8FG_F32;
+  p.b_tile = b_tile ? 1 : 0;
+  p.wait_limit = wait_limit_cycles();
+  p.status = device_status_word();
+  const int tiles = p.m_tiles * p.n_tiles;
+  const int grid = tiles < device_sm_count() ? tiles : device_sm_count();
+  blockscaled_gemm_kernel<false><<<grid, NUM_THREADS, kSmemBytes, st>>>(mA, mB, p);
+  return cudaGetLastError() == cudaSuccess ? FP8FG_OK : FP8FG_ERR_CUDA;
+}
+
+fp8fg_status launch_grouped_gemm(const uint8_t* a, const float* sa, const int32_t* offsets,
+                                 int32_t E, int64_t total_rows, const uint8_t* b, const float* sb,
+                                 void* c, fp8fg_dtype ct, int64_t N, int64_t K, cudaStream_t st) {
+  CUtensorMap mA, mB;
+  // an empty A (no rows) still needs a valid map: point it at one row
+  if (!make_maps(&mA, &mB, a, total_rows > 0 ? total_rows : 1, b, E, N, K)) return FP8FG_ERR_CUDA;
+  if (set_smem_attr<true>() != cudaSuccess) return FP8FG_ERR_CUDA;
+  GemmParams p{};
+  p.sa = sa;
+  p.sb = sb;
+  p.c = c;
+  p.offsets = offsets;
+  p.M = static_cast<int>(total_rows);
+  p.N = static_cast<int>(N);
+  p.K = static_cast<int>(K);
+  p.nkb = static_cast<int>(K / BK);
+  p.m_tiles = 0;
+  p.n_tiles = static_cast<int>((N + BN - 1) / BN);
+  p.E = E;
+  p.c_f32 = ct == FP8FG_F32;
+  p.b_tile = 0;
+  p.wait_limit = wait_limit_cycles();
+  p.status = device_status_word();
+  blockscaled_gemm_kernel<true><<<device_sm_count(), NUM_THREADS, kSmemBytes, st>>>(mA, mB, p);
+  return cudaGetLastError() == cudaSuccess ? FP8FG_OK : FP8FG_ERR_CUDA;
+}
+
+cudaError_t launch_wait_timeout_selftest(uint32_t limit_cycles, cudaStream_t st) {
+  wait_timeout_selftest_kernel<<<1, 32, 0, st>>>(static_cast<long long>(limit_cycles),
+                                                 device_status_word());
+  return cudaGetLastError();
+}
+
+}  // namespace fp8fg

@@ -1,0 +1,42 @@
+// Internal launcher declarations shared by the C-ABI layer and the kernels.
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "fp8fg.h"
+
+namespace fp8fg {
+
+// Number of SMs of the current device (cached per device).
+int device_sm_count();
+// Cycle limit applied to every pipeline wait of the next launches.
+long long wait_limit_cycles();
+// Device address of the library status word on the current device.
+int* device_status_word();
+
+cudaError_t launch_act_quant_rows(const void* x, fp8fg_dtype xt, int64_t M, int64_t K, uint8_t* q,
+                                  float* s, bool pow2, cudaStream_t st);
+cudaError_t launch_act_quant_cols(const void* x, fp8fg_dtype xt, int64_t M, int64_t K, uint8_t* qt,
+                                  float* st_, bool pow2, cudaStream_t st);
+cudaError_t launch_weight_quant(const void* w, fp8fg_dtype wt, int64_t N, int64_t K, uint8_t* q,
+                                float* s, uint8_t* qt, float* st_, bool pow2, cudaStream_t st);
+
+// Dense block-scaled GEMM (b_tile: B carries 1x128 tile scales).
+fp8fg_status launch_gemm(const uint8_t* a, const float* sa, const uint8_t* b, const float* sb,
+                         void* c, fp8fg_dtype ct, int64_t M, int64_t N, int64_t K, bool b_tile,
+                         cudaStream_t st);
+// Grouped block-scaled GEMM over contiguous expert row groups.
+fp8fg_status launch_grouped_gemm(const uint8_t* a, const float* sa, const int32_t* offsets,
+                                 int32_t E, int64_t total_rows, const uint8_t* b, const float* sb,
+                                 void* c, fp8fg_dtype ct, int64_t N, int64_t K, cudaStream_t st);
+// Failure-detection self-test: one wait that nothing completes.
+cudaError_t launch_wait_timeout_selftest(uint32_t limit_cycles, cudaStream_t st);
+
+// Encode a 2D/3D uint8 tensor map (innermost dimension first) with 128-byte
+// swizzling and zero fill; returns false if the driver rejects it.
+bool encode_tensor_map_u8(CUtensorMap* map, const void* base, int rank, const uint64_t* dims,
+                          const uint64_t* strides_bytes, const uint32_t* box);
+
+}  // namespace fp8fg

@@ -1,0 +1,166 @@
+/*
+ * fp8fg.h -- C ABI of libfp8fg.so: fine-grained E4M3 quantisation and
+ * block-scaled FP8 GEMMs with per-128-K FP32 promotion, for NVIDIA B300
+ * (sm_103a).
+ *
+ * The method is the FP8 mixed-precision training scheme described on the
+ * scraped DeepSeek-V3 pages (cited as page + passage):
+ *   page 1 = xn--9g3bo1gtkw0l8ubf92bgle.kr qna #85187,
+ *   page 2 = inprokorea.com free #735329,
+ *   page 5 = inprokorea.com free #890463.
+ *
+ * Conventions for every entry point
+ *   - Memory: every pointer argument is a DEVICE pointer, except where stated.
+ *     The caller owns and allocates all of it; the library allocates nothing
+ *     per call.  (It keeps one device status word and, per device, a cached
+ *     SM count; both live until the library is unloaded.)
+ *   - Layout: tensors are dense, contiguous, row-major; no leading dimension.
+ *   - Alignment: every pointer must be 16-byte aligned.
+ *   - Sizes: int64_t, each dimension below 2^31; K % 128 == 0 everywhere.
+ *   - Stream: `stream` is a cudaStream_t (NULL = the legacy default stream).
+ *     Every call is asynchronous on it.  The return value reports argument
+ *     validation and launch errors only; no kernel is launched when the
+ *     arguments are rejected.
+ *   - Device-detected errors (a pipeline wait that ran out of its cycle limit,
+ *     bad expert offsets) are written to the library status word; the kernel
+ *     then stops early without trapping.  fp8_get_device_status() reports and
+ *     clears it.
+ *   - There is no CPU fallback: without a CUDA device every call returns
+ *     FP8FG_ERR_CUDA (after validation).
+ */
+#ifndef FP8FG_H_
+#define FP8FG_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  FP8FG_OK = 0,
+  FP8FG_ERR_INVALID_ARG = 1,      /* null pointer, negative size, unknown flag or dtype */
+  FP8FG_ERR_UNSUPPORTED_SHAPE = 2,/* a dimension breaks a divisibility or size rule */
+  FP8FG_ERR_MISALIGNED = 3,       /* a pointer is not 16-byte aligned */
+  FP8FG_ERR_CUDA = 4,             /* a CUDA runtime/driver call failed (no device, launch) */
+  FP8FG_ERR_TIMEOUT = 5,          /* device: a pipeline wait exceeded its cycle limit */
+  FP8FG_ERR_BAD_OFFSETS = 6       /* device: expert offsets not 0..total, non-decreasing */
+} fp8fg_status;
+
+typedef enum { FP8FG_BF16 = 0, FP8FG_F32 = 1 } fp8fg_dtype;
+
+/* flag bits */
+#define FP8FG_POW2 1u          /* scales rounded up to an integral power of 2 */
+#define FP8FG_TRANSPOSE 2u     /* act_quant: 128x1 tiles, transposed output */
+#define FP8FG_B_TILE1x128 4u   /* GEMM: B carries 1x128 tile scales [N, K/128] */
+
+/*
+ * fp8_act_quant -- online 1x128 tile quantisation of activations to E4M3.
+ * Source: page 1, Figure 7 (a) (one scale per token per 128 channels) and the
+ * "Storage Format: float32" passage; page 2, passage on computing the maximum
+ * absolute value online per 1x128 tile; pages 1 and 2, passage making the
+ * scales integral powers of 2 for some activations (FP8FG_POW2); page 5,
+ * backward-pass passage re-quantising into 128x1 tiles (FP8FG_TRANSPOSE).
+ *
+ * x      [M, K] BF16 or FP32 (x_dtype), row-major.
+ * default: q [M, K] E4M3 codes (uint8), s [M, K/128] FP32, both row-major.
+ *          Tile (r, t) = x[r, 128t .. 128t+127].
+ * FP8FG_TRANSPOSE: requires M % 128 == 0; q [K, M], s [K, M/128] (row-major),
+ *          tile (k, i) = x[128i .. 128i+127, k], i.e. act_quant of x^T.
+ * Per tile: amax = max|x| (floored at 2^-64); s = amax/448 (IEEE FP32 divide);
+ *          codes = E4M3_rne_satfinite(x * (448/amax)), one FP32 multiply each.
+ *          FP8FG_POW2: s = 2^ceil(log2(amax/448)), multiplier 1/s (exact).
+ * M may be 0 (nothing is launched).  Flags other than POW2|TRANSPOSE are
+ * rejected.
+ */
+fp8fg_status fp8_act_quant(const void* x, fp8fg_dtype x_dtype, int64_t M, int64_t K,
+                           uint8_t* q, float* s, unsigned flags, void* stream);
+
+/*
+ * fp8_weight_quant -- online 128x128 block quantisation of weights to E4M3.
+ * Source: page 1, Figure 7 (a) (one scale per 128 input x 128 output
+ * channels) and "Storage Format" passage; page 2, online-amax passage.
+ *
+ * w    [N, K] BF16 or FP32, N % 128 == 0, K % 128 == 0.
+ * q    [N, K] codes; s [N/128, K/128] FP32 (block (i, j) = rows 128i.., cols 128j..).
+ * q_t  optional (NULL to skip) [K, N] codes = q transposed; s_t [K/128, N/128]
+ *      = s transposed (both or neither).  These feed the Dgrad GEMM.
+ * Scale rule as fp8_act_quant, per block; FP8FG_POW2 is honoured.
+ */
+fp8fg_status fp8_weight_quant(const void* w, fp8fg_dtype w_dtype, int64_t N, int64_t K,
+                              uint8_t* q, float* s, uint8_t* q_t, float* s_t, unsigned flags,
+                              void* stream);
+
+/*
+ * fp8_blockscaled_gemm -- C = A . B^T with per-128-K promotion.
+ * Source: page 2, promotion passage (partial results copied to FP32 registers
+ * and accumulated there; the garbled interval is read as 128, the K group of
+ * the scales) and Figure 6 (Fprop, Dgrad and Wgrad all in FP8); page 2,
+ * passage multiplying the per-group K scales in during dequantisation.
+ *
+ * a  [M, K] E4M3 codes, sa [M, K/128] FP32 (1x128 tiles).
+ * b  [N, K] E4M3 codes; sb [N/128, K/128] FP32 (128x128 blocks, requires
+ *    N % 128 == 0) or, with FP8FG_B_TILE1x128, sb [N, K/128] (1x128 tiles,
+ *    requires N % 16 == 0).
+ * c  [M, N] BF16 or FP32 (c_dtype), row-major.
+ * C[m,n] = sum_kb P_kb[m,n] * sa[m,kb] * sb(n,kb), P_kb the tensor-core product
+ * over K group kb; each P_kb is scaled and added into an FP32 accumulator; the
+ * output is rounded once (RNE to BF16, or stored as FP32).
+ * M >= 0 arbitrary (0: nothing launched); N >= 16; K >= 128.
+ */
+fp8fg_status fp8_blockscaled_gemm(const uint8_t* a, const float* sa, const uint8_t* b,
+                                  const float* sb, void* c, fp8fg_dtype c_dtype, int64_t M,
+                                  int64_t N, int64_t K, unsigned flags, void* stream);
+
+/*
+ * fp8_grouped_gemm -- fp8_blockscaled_gemm per routed expert over contiguous
+ * row groups.  Source: page 2, passage quantising the activation before the
+ * MoE up-projection for FP8 Fprop; page 5, MoE configuration passage (256
+ * routed experts, 8 active per token, expert hidden size 2048).
+ *
+ * a        [total_rows, K] codes, rows grouped by expert; sa [total_rows, K/128].
+ * offsets  DEVICE int32 [E+1]: expert e owns rows offsets[e] .. offsets[e+1]-1.
+ *          Must satisfy offsets[0] == 0, non-decreasing, offsets[E] == total_rows;
+ *          checked on the device (FP8FG_ERR_BAD_OFFSETS, nothing written).
+ * b        [E, N, K] codes; sb [E, N/128, K/128] FP32 (128x128 blocks).
+ * c        [total_rows, N] BF16 or FP32.  Rows of empty experts: none.
+ * Requires 1 <= E <= 1024, N % 128 == 0; flags must be 0.
+ */
+fp8fg_status fp8_grouped_gemm(const uint8_t* a, const float* sa, const int32_t* offsets,
+                              int32_t E, int64_t total_rows, const uint8_t* b, const float* sb,
+                              void* c, fp8fg_dtype c_dtype, int64_t N, int64_t K, unsigned flags,
+                              void* stream);
+
+/*
+ * fp8_get_device_status -- synchronises `stream`, then returns and clears the
+ * library status word (FP8FG_OK, FP8FG_ERR_TIMEOUT or FP8FG_ERR_BAD_OFFSETS);
+ * FP8FG_ERR_CUDA if the synchronisation itself failed.
+ */
+fp8fg_status fp8_get_device_status(void* stream);
+
+/* Short English description of a status code (static storage). */
+const char* fp8fg_status_string(fp8fg_status status);
+
+/* ABI version of this header (bumped on any signature change). */
+int fp8fg_abi_version(void);
+
+/*
+ * fp8fg_set_wait_limit -- cycle limit of every pipeline wait in later launches
+ * (default 2^32 cycles, about two seconds; 0 restores the default).  Also read
+ * once from the environment variable FP8FG_WAIT_LIMIT_CYCLES.  Host-side only.
+ */
+void fp8fg_set_wait_limit(uint64_t cycles);
+
+/*
+ * fp8fg_selftest_wait_timeout -- failure-detection self-test.  Launches one
+ * CTA that waits on an mbarrier nothing will ever arrive on, with the given
+ * cycle limit (1 .. 2^31), so the wait must give up and record
+ * FP8FG_ERR_TIMEOUT.  Read the result with fp8_get_device_status().
+ */
+fp8fg_status fp8fg_selftest_wait_timeout(uint32_t limit_cycles, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FP8FG_H_ */

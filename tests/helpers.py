@@ -1,0 +1,85 @@
+"""Shared helpers for the parity tests (oracle side on the CPU, library side on the GPU)."""
+
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import oracle
+import synth
+
+GUARD = 4096      # bytes of canary on each side of a guarded output
+
+
+def oracle_act_quant_rows(x_f32: np.ndarray, pow2=False, rows_per_chunk=2048):
+    """oracle.act_quant over row chunks (tiles never cross rows, so this is exact)."""
+    M, K = x_f32.shape
+    q = np.empty((M, K), np.uint8)
+    s = np.empty((M, K // 128), np.float32)
+    for r in range(0, M, rows_per_chunk):
+        q[r:r + rows_per_chunk], s[r:r + rows_per_chunk] = oracle.act_quant(
+            x_f32[r:r + rows_per_chunk], pow2=pow2)
+    return q, s
+
+
+def oracle_act_quant_cols(x_f32: np.ndarray, pow2=False, cols_per_chunk=1024):
+    """oracle.act_quant_t over column chunks (tiles never cross columns)."""
+    M, K = x_f32.shape
+    qt = np.empty((K, M), np.uint8)
+    st = np.empty((K, M // 128), np.float32)
+    for c in range(0, K, cols_per_chunk):
+        qt[c:c + cols_per_chunk], st[c:c + cols_per_chunk] = oracle.act_quant_t(
+            np.ascontiguousarray(x_f32[:, c:c + cols_per_chunk]), pow2=pow2)
+    return qt, st
+
+
+def oracle_weight_quant(w_f32: np.ndarray, pow2=False, rows_per_chunk=1024):
+    """oracle.weight_quant over strips of whole 128-row blocks."""
+    N, K = w_f32.shape
+    q = np.empty((N, K), np.uint8)
+    s = np.empty((N // 128, K // 128), np.float32)
+    for r in range(0, N, rows_per_chunk):
+        q[r:r + rows_per_chunk], s[r // 128:(r + rows_per_chunk) // 128] = oracle.weight_quant(
+            w_f32[r:r + rows_per_chunk], pow2=pow2)
+    return q, s
+
+
+def normwise_rel_err(c_gpu, c_ref: np.ndarray) -> float:
+    g = c_gpu.detach().float().cpu().numpy().astype(np.float64) if isinstance(c_gpu, torch.Tensor) \
+        else np.asarray(c_gpu, np.float64)
+    return float(np.linalg.norm(g - c_ref) / np.linalg.norm(c_ref))
+
+
+def to_dev(a, dev="cuda"):
+    if isinstance(a, torch.Tensor):
+        return a.to(dev).contiguous()
+    return torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+
+
+def guarded_empty(shape, dtype, fill_byte=0xA5, dev="cuda"):
+    """An output tensor with canary bytes before and after it in one allocation."""
+    nbytes = int(np.prod(shape)) * torch.empty((), dtype=dtype).element_size()
+    raw = torch.full((GUARD + nbytes + GUARD,), fill_byte, dtype=torch.uint8, device=dev)
+    body = raw[GUARD:GUARD + nbytes].view(dtype).view(shape)
+    return raw, body
+
+
+def guards_intact(raw: torch.Tensor, fill_byte=0xA5) -> bool:
+    head = raw[:GUARD]
+    tail = raw[-GUARD:]
+    return bool((head == fill_byte).all().item() and (tail == fill_byte).all().item())
+
+
+def f32(t: torch.Tensor) -> np.ndarray:
+    return synth.bf16_to_f32(t)
+
+
+def oracle_gemm_chunked(qa, sa, qb, sb, b_tile=False, chunk=2048) -> np.ndarray:
+    """oracle.gemm over column chunks of B (output columns are independent)."""
+    N = qb.shape[0]
+    parts = []
+    for c0 in range(0, N, chunk):
+        c1 = min(N, c0 + chunk)
+        sbc = sb[c0:c1] if b_tile else sb[c0 // 128:(c1 + 127) // 128]
+        parts.append(oracle.gemm(qa, sa, qb[c0:c1], sbc, b_tile=b_tile))
+    return np.concatenate(parts, axis=1)
