@@ -45,7 +45,7 @@ TRAFFIC_FILE = os.path.join(ROOT, "profiles", "gemm_fprop_traffic.json")
 def parse():
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
-    p.add_argument("--steps", type=int, default=200)
+    p.add_argument("--steps", type=int, default=2000)
     p.add_argument("--warmup", type=int, default=10)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--e2e-steps", type=int, default=20)
@@ -85,67 +85,65 @@ def traffic_for_current_kernel():
 
 # ----------------------------------------------------------------- clocks
 class ClockSampler:
-    """Polls NVML (SM clock, power, throttle reasons) on a thread during the timed region."""
+    """Samples SM clock, power and clock-event reasons with nvidia-smi during the timed region."""
 
-    def __init__(self, device_index: int, period_s: float = 0.005):
-        self.samples = []
-        self.period = period_s
-        self.ok = False
-        try:
-            import pynvml
-            pynvml.nvmlInit()
-            self.nv = pynvml
-            self.h = pynvml.nvmlDeviceGetHandleByIndex(device_index)
-            self.max_mhz = pynvml.nvmlDeviceGetMaxClockInfo(self.h, pynvml.NVML_CLOCK_SM)
-            self.ok = True
-        except Exception:
-            self.max_mhz = None
-        self._stop = threading.Event()
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def _run(self):
-        nv = self.nv
-        while not self._stop.is_set():
-            try:
-                mhz = nv.nvmlDeviceGetClockInfo(self.h, nv.NVML_CLOCK_SM)
-                reasons = nv.nvmlDeviceGetCurrentClocksEventReasons(self.h)
-                self.samples.append((mhz, reasons))
-            except Exception:
-                pass
-            time.sleep(self.period)
+    def __init__(self, device_index: int, period_ms: int = 50):
+        self.cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                    "-i", str(device_index), "-lms", str(period_ms)]
+        self.proc = None
+        self.out = b""
+        self.error = None
 
     def __enter__(self):
-        if self.ok:
-            self.t = threading.Thread(target=self._run, daemon=True)
-            self.t.start()
+        import subprocess
+        try:
+            self.proc = subprocess.Popen(self.cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)          # let the first samples land before the timed work starts
+        except Exception as e:       # no nvidia-smi: the line says so
+            self.error = repr(e)
         return self
 
     def __exit__(self, *exc):
-        if self.ok:
-            self._stop.set()
-            self.t.join()
+        if self.proc is not None:
+            time.sleep(0.1)
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except Exception:
+                self.proc.kill()
+                self.out, _ = self.proc.communicate()
 
     def summary(self):
-        if not self.ok:
-            return None
-        nv = self.nv
-        names = {
-            "gpu_idle": getattr(nv, "nvmlClocksEventReasonGpuIdle", 0x1),
-            "applications_clocks_setting": getattr(nv, "nvmlClocksEventReasonApplicationsClocksSetting", 0x2),
-            "sw_power_cap": getattr(nv, "nvmlClocksEventReasonSwPowerCap", 0x4),
-            "hw_slowdown": getattr(nv, "nvmlClocksEventReasonHwSlowdown", 0x8),
-            "sync_boost": getattr(nv, "nvmlClocksEventReasonSyncBoost", 0x10),
-            "sw_thermal_slowdown": getattr(nv, "nvmlClocksEventReasonSwThermalSlowdown", 0x20),
-            "hw_thermal_slowdown": getattr(nv, "nvmlClocksEventReasonHwThermalSlowdown", 0x40),
-            "hw_power_brake_slowdown": getattr(nv, "nvmlClocksEventReasonHwPowerBrakeSlowdown", 0x80),
-        }
+        if self.proc is None:
+            return {"error": self.error or "nvidia-smi not started"}
+        rows = []
+        for line in self.out.decode(errors="replace").splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) != 8:
+                continue
+            try:
+                rows.append((float(f[0]), float(f[1]), float(f[2]), f[3:]))
+            except ValueError:
+                continue
+        if not rows:
+            return {"error": "no samples"}
+        # samples under load: power well above idle (the timed region is all GPU work)
+        pmax = max(r[2] for r in rows)
+        load = [r for r in rows if r[2] >= 0.5 * pmax] or rows
+        names = ["active_mask", "hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown",
+                 "sw_power_cap"]
         seen = set()
-        for _, r in self.samples:
-            for k, bit in names.items():
-                if r & bit:
-                    seen.add(k)
-        mhz = [m for m, _ in self.samples]
-        return {"sm_mhz": statistics.median(mhz) if mhz else None, "sm_max_mhz": self.max_mhz,
-                "samples": len(mhz), "reasons": sorted(seen), "source": "nvml"}
+        for r in load:
+            for n, v in zip(names[1:], r[3][1:]):
+                if v.lower() == "active":
+                    seen.add(n)
+        return {"sm_mhz": statistics.median(r[0] for r in load), "sm_max_mhz": rows[0][1],
+                "power_w_max": pmax, "samples": len(rows), "samples_under_load": len(load),
+                "reasons": sorted(seen), "source": "nvidia-smi -lms 50"}
 
 
 # ------------------------------------------------------------ our GPU arm
@@ -262,7 +260,12 @@ def run_ours(args, rank, world):
                "d2h_bytes_per_step": c_h.numel() * 2}
 
     pk = peaks()
-    fp8_peak = 2.0 * pk["bf16"]
+    # The GEMM is timed inside a long run of back-to-back steps (seconds of load under the
+    # power cap), so its denominator is the sustained figure: FP8 dense = 2 x the measured
+    # sustained BF16 matmul rate (the nominal FP8:BF16 ratio 4.5:2.25).  The burst-derived
+    # and nominal (4500 TF/s) fractions are reported beside it.
+    fp8_peak = 2.0 * pk["bf16_sustained"]
+    fp8_burst = 2.0 * pk["bf16"]
     gemm_tflops = FLOPS / (t_mm * 1e-3) / 1e12
     aq_bytes = M * K * 2 + M * K + M * (K // 128) * 4
     wq_bytes = N * K * 2 + N * K + (N // 128) * (K // 128) * 4
@@ -286,7 +289,8 @@ def run_ours(args, rank, world):
                      "achieved": round(gemm_tflops, 2),
                      "peak": round(fp8_peak, 1), "unit": "TFLOP/s",
                      "frac": round(gemm_tflops / fp8_peak, 4),
-                     "peak_source": f"2 x bf16 burst of {pk['source']} ({pk['bf16']} TF/s)",
+                     "peak_source": f"2 x bf16 sustained, {pk['source']} ({pk['bf16_sustained']} TF/s)",
+                     "frac_of_burst": round(gemm_tflops / fp8_burst, 4),
                      "frac_of_nominal_4500": round(gemm_tflops / 4500.0, 4),
                      "traffic": traffic_for_current_kernel(),
                      "algorithmic_bytes": gemm_bytes},

@@ -132,7 +132,7 @@ __device__ __forceinline__ Tile tile_of(int t, const GemmParams& p, const Smem& 
   return r;
 }
 
-template <bool GROUPED>
+template <bool GROUPED, bool BTILE>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     blockscaled_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                             const __grid_constant__ CUtensorMap tmB, const GemmParams p) {
@@ -287,6 +287,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const int half = warp >> 2;                     // N half of the tile
     const int tid_h = threadIdx.x & 127;            // index within the half's warpgroup
     const int n_blocks = p.N / 128;                 // block-mode scale rows per expert
+    const uint32_t lane_taddr = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + half * 128;
     uint32_t it = 0;
     bool ok = true;
     for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
@@ -295,32 +296,29 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const bool row_ok = row < tl.row_end;
       const int col_h = tl.n0 + half * 128;         // first column of this half
       const bool half_ok = col_h < p.N;
+      // rows and columns past the end read valid scales (row 0 / the last
+      // column) and are never stored
       const float* sa_row = p.sa + static_cast<int64_t>(row_ok ? row : 0) * nkb;
-      const float* sb_ptr;
-      if (p.b_tile) {
-        const int col = col_h + tid_h;
-        sb_ptr = p.sb + static_cast<int64_t>(col < p.N ? col : 0) * nkb;
-      } else {
-        sb_ptr = p.sb + (static_cast<int64_t>(tl.e) * n_blocks + (half_ok ? col_h / 128 : 0)) * nkb;
-      }
-      const bool sb_ok = p.b_tile ? (col_h + tid_h < p.N) : half_ok;
+      const float* sb_ptr =
+          BTILE ? p.sb + static_cast<int64_t>(min(col_h + tid_h, p.N - 1)) * nkb
+                : p.sb + (static_cast<int64_t>(tl.e) * n_blocks + (half_ok ? col_h / 128 : 0)) * nkb;
 
       uint64_t acc[64];
 #pragma unroll
       for (int j = 0; j < 64; ++j) acc[j] = 0;
 
-      float sa_next = row_ok ? __ldg(sa_row) : 0.0f;
-      float sb_next = sb_ok ? __ldg(sb_ptr) : 0.0f;
+      float sa_next = __ldg(sa_row);
+      float sb_next = __ldg(sb_ptr);
       for (int kb = 0; kb < nkb; ++kb, ++it) {
         const float sa_cur = sa_next, sb_cur = sb_next;
         if (kb + 1 < nkb) {
-          sa_next = row_ok ? __ldg(sa_row + kb + 1) : 0.0f;
-          sb_next = sb_ok ? __ldg(sb_ptr + kb + 1) : 0.0f;
+          sa_next = __ldg(sa_row + kb + 1);
+          sb_next = __ldg(sb_ptr + kb + 1);
         }
         const uint32_t buf = it & 1, bpar = (it >> 1) & 1;
         const bool got =
             mbar_wait(smem_u32(&sm.tfull_bar[buf]), bpar, p.wait_limit, abort_flag, p.status);
-        if (p.b_tile) {
+        if constexpr (BTILE) {
           // publish this slice's column scales to the half; the barrier also
           // takes a vote so that all 128 threads leave together on an abort
           sm.sbt[half][it & 1][tid_h] = sb_cur;
@@ -333,9 +331,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           break;
         }
         tc_fence_after();
-        const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + buf * BN +
-                               half * 128;
-        if (!p.b_tile) {
+        const uint32_t taddr = lane_taddr + buf * BN;
+        if constexpr (!BTILE) {
           const float s = sa_cur * sb_cur;
           const uint64_t s2 = pack2(__float_as_uint(s), __float_as_uint(s));
 #pragma unroll
@@ -448,10 +445,10 @@ bool make_maps(CUtensorMap* mA, CUtensorMap* mB, const uint8_t* a, int64_t rowsA
   return encode_tensor_map_u8(mB, b, 3, dB, sB, boxB);
 }
 
-template <bool GROUPED>
+template <bool GROUPED, bool BTILE>
 cudaError_t set_smem_attr() {
   static const cudaError_t e = cudaFuncSetAttribute(
-      blockscaled_gemm_kernel<GROUPED>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+      blockscaled_gemm_kernel<GROUPED, BTILE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
       static_cast<int>(kSmemBytes));
   return e;
 }
@@ -463,7 +460,8 @@ fp8fg_status launch_gemm(const uint8_t* a, const float* sa, const uint8_t* b, co
                          cudaStream_t st) {
   CUtensorMap mA, mB;
   if (!make_maps(&mA, &mB, a, M, b, 0, N, K)) return FP8FG_ERR_CUDA;
-  if (set_smem_attr<false>() != cudaSuccess) return FP8FG_ERR_CUDA;
+  if ((b_tile ? set_smem_attr<false, true>() : set_smem_attr<false, false>()) != cudaSuccess)
+    return FP8FG_ERR_CUDA;
   GemmParams p{};
   p.sa = sa;
   p.sb = sb;
@@ -482,7 +480,10 @@ fp8fg_status launch_gemm(const uint8_t* a, const float* sa, const uint8_t* b, co
   p.status = device_status_word();
   const int tiles = p.m_tiles * p.n_tiles;
   const int grid = tiles < device_sm_count() ? tiles : device_sm_count();
-  blockscaled_gemm_kernel<false><<<grid, NUM_THREADS, kSmemBytes, st>>>(mA, mB, p);
+  if (b_tile)
+    blockscaled_gemm_kernel<false, true><<<grid, NUM_THREADS, kSmemBytes, st>>>(mA, mB, p);
+  else
+    blockscaled_gemm_kernel<false, false><<<grid, NUM_THREADS, kSmemBytes, st>>>(mA, mB, p);
   return cudaGetLastError() == cudaSuccess ? FP8FG_OK : FP8FG_ERR_CUDA;
 }
 
@@ -492,7 +493,7 @@ fp8fg_status launch_grouped_gemm(const uint8_t* a, const float* sa, const int32_
   CUtensorMap mA, mB;
   // an empty A (no rows) still needs a valid map: point it at one row
   if (!make_maps(&mA, &mB, a, total_rows > 0 ? total_rows : 1, b, E, N, K)) return FP8FG_ERR_CUDA;
-  if (set_smem_attr<true>() != cudaSuccess) return FP8FG_ERR_CUDA;
+  if (set_smem_attr<true, false>() != cudaSuccess) return FP8FG_ERR_CUDA;
   GemmParams p{};
   p.sa = sa;
   p.sb = sb;
@@ -509,7 +510,7 @@ fp8fg_status launch_grouped_gemm(const uint8_t* a, const float* sa, const int32_
   p.b_tile = 0;
   p.wait_limit = wait_limit_cycles();
   p.status = device_status_word();
-  blockscaled_gemm_kernel<true><<<device_sm_count(), NUM_THREADS, kSmemBytes, st>>>(mA, mB, p);
+  blockscaled_gemm_kernel<true, false><<<device_sm_count(), NUM_THREADS, kSmemBytes, st>>>(mA, mB, p);
   return cudaGetLastError() == cudaSuccess ? FP8FG_OK : FP8FG_ERR_CUDA;
 }
 
