@@ -138,6 +138,26 @@ __device__ __forceinline__ void mma_commit(uint32_t bar) {
                : "memory");
 }
 
+// Warp-converged issue.  The whole warp executes these; elect.sync picks one
+// lane (always the same one while the warp is converged, so its commits track
+// its own MMAs) and only that lane issues.  Keeping the warp converged lets the
+// operands stay warp-uniform: issuing from a diverged single thread measured
+// ~90 cycles per MMA, more than an M128 N128 K32 MMA takes to execute.
+__device__ __forceinline__ void mma_f8_elect(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc,
+                                             uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p, e;\n setp.ne.b32 p, %4, 0;\n elect.sync _|e, 0xffffffff;\n"
+      " @e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n}\n" ::"r"(tmem_d),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void mma_commit_elect(uint32_t bar) {
+  asm volatile(
+      "{\n .reg .pred e;\n elect.sync _|e, 0xffffffff;\n"
+      " @e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n}\n" ::"r"(
+          bar)
+      : "memory");
+}
 // 32 lanes x 32 consecutive 32-bit TMEM columns -> 32 registers per thread.
 __device__ __forceinline__ void tmem_ld_32cols(uint32_t taddr, uint32_t (&r)[32]) {
   asm volatile(

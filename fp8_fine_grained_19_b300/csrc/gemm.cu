@@ -11,10 +11,11 @@
 // B300 design (one persistent CTA per SM, 384 threads, 1 CTA/SM):
 //   warp 8      TMA producer: one 128x128 A tile + one 256x128 B tile of E4M3
 //               codes per 128-K slice into a 4-stage ring (128-byte swizzle).
-//   warp 9      MMA issuer: one thread issues 4 x tcgen05.mma (M128 N256 K32,
-//               kind::f8f6f4, FP32 accumulate) per slice into one of two TMEM
-//               buffers (2 x 256 columns), then commits to the stage's "empty"
-//               barrier and the buffer's "full" barrier.
+//   warp 9      MMA issuer: one elected lane of the converged warp issues
+//               4 x tcgen05.mma (M128 N256 K32, kind::f8f6f4, FP32 accumulate)
+//               per slice into one of two TMEM buffers (2 x 256 columns), then
+//               commits to the stage's "empty" barrier and the buffer's "full"
+//               barrier.
 //   warps 0-7   promotion/epilogue: warp w reads TMEM lanes 32(w%4).. (its 32
 //               rows) and columns 128(w/4).. (its half of N) of the finished
 //               buffer with tcgen05.ld, frees the buffer, and does
@@ -218,37 +219,40 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   if (warp >= NUM_EPI_WARPS) {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(REGS_PRODUCER));
     if (warp == PRODUCER_WARP) {
-    // --------------------------------------------------------- TMA producer
-    if (lane == 0) {
-      int stage = 0;
-      uint32_t phase = 0;
-      uint32_t issued = 0, issued_parity = 0;   // per-stage bits
-      for (int t = blockIdx.x; t < num_tiles && !*abort_flag; t += gridDim.x) {
-        const Tile tl = tile_of<GROUPED>(t, p, sm);
-        for (int kb = 0; kb < nkb; ++kb) {
-          if (!mbar_wait(smem_u32(&sm.empty_bar[stage]), phase ^ 1, p.wait_limit, abort_flag, p.status))
-            break;
-          const uint32_t fb = smem_u32(&sm.full_bar[stage]);
-          mbar_arrive_expect_tx(fb, A_BYTES + B_BYTES);
-          tma_load_2d(smem_u32(sm.a[stage]), &tmA, fb, kb * BK, tl.m0);
-          if constexpr (GROUPED)
-            tma_load_3d(smem_u32(sm.b[stage]), &tmB, fb, kb * BK, tl.n0, tl.e);
-          else
-            tma_load_2d(smem_u32(sm.b[stage]), &tmB, fb, kb * BK, tl.n0);
-          issued |= 1u << stage;
-          issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
-          if (++stage == STAGES) { stage = 0; phase ^= 1; }
+      // ------------------------------------------------------- TMA producer
+      if (lane == 0) {
+        int stage = 0;
+        uint32_t phase = 0;
+        uint32_t issued = 0, issued_parity = 0;   // per-stage bits
+        for (int t = blockIdx.x; t < num_tiles && !*abort_flag; t += gridDim.x) {
+          const Tile tl = tile_of<GROUPED>(t, p, sm);
+          for (int kb = 0; kb < nkb; ++kb) {
+            if (!mbar_wait(smem_u32(&sm.empty_bar[stage]), phase ^ 1, p.wait_limit, abort_flag,
+                           p.status))
+              break;
+            const uint32_t fb = smem_u32(&sm.full_bar[stage]);
+            mbar_arrive_expect_tx(fb, A_BYTES + B_BYTES);
+            tma_load_2d(smem_u32(sm.a[stage]), &tmA, fb, kb * BK, tl.m0);
+            if constexpr (GROUPED)
+              tma_load_3d(smem_u32(sm.b[stage]), &tmB, fb, kb * BK, tl.n0, tl.e);
+            else
+              tma_load_2d(smem_u32(sm.b[stage]), &tmB, fb, kb * BK, tl.n0);
+            issued |= 1u << stage;
+            issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
+            if (++stage == STAGES) { stage = 0; phase ^= 1; }
+          }
         }
+        // never leave the CTA with a bulk copy still landing in shared memory
+        volatile int never = 0;
+        for (int s = 0; s < STAGES; ++s)
+          if (issued & (1u << s))
+            mbar_wait(smem_u32(&sm.full_bar[s]), (issued_parity >> s) & 1, p.wait_limit, &never,
+                      p.status);
       }
-      // never leave the CTA with a bulk copy still landing in shared memory
-      volatile int never = 0;
-      for (int s = 0; s < STAGES; ++s)
-        if (issued & (1u << s))
-          mbar_wait(smem_u32(&sm.full_bar[s]), (issued_parity >> s) & 1, p.wait_limit, &never, p.status);
-    }
-  } else if (warp == MMA_WARP) {
-    // ----------------------------------------------------------- MMA issuer
-    if (lane == 0) {
+    } else if (warp == MMA_WARP) {
+      // --------------------------------------------------------- MMA issuer
+      // The whole warp runs the loop: lane 0 waits on the barriers and
+      // broadcasts the outcome, one elected lane issues.
       int stage = 0;
       uint32_t phase = 0;
       uint32_t it = 0;                              // slice counter (TMEM buffers)
@@ -256,8 +260,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
         for (int kb = 0; kb < nkb; ++kb, ++it) {
           const uint32_t buf = it & 1, bpar = (it >> 1) & 1;
-          if (!mbar_wait(smem_u32(&sm.tempty_bar[buf]), bpar ^ 1, p.wait_limit, abort_flag, p.status) ||
-              !mbar_wait(smem_u32(&sm.full_bar[stage]), phase, p.wait_limit, abort_flag, p.status)) {
+          int got = 0;
+          if (lane == 0)
+            got = mbar_wait(smem_u32(&sm.tempty_bar[buf]), bpar ^ 1, p.wait_limit, abort_flag,
+                            p.status) &&
+                  mbar_wait(smem_u32(&sm.full_bar[stage]), phase, p.wait_limit, abort_flag,
+                            p.status);
+          if (!__shfl_sync(0xFFFFFFFFu, got, 0)) {
             ok = false;
             break;
           }
@@ -267,18 +276,19 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           const uint32_t d = tmem_base + buf * BN;
 #pragma unroll
           for (int k = 0; k < BK / 32; ++k)
-            mma_f8(d, smem_desc_sw128(a0 + 32 * k), smem_desc_sw128(b0 + 32 * k), IDESC,
-                   k > 0 ? 1u : 0u);
-          mma_commit(smem_u32(&sm.empty_bar[stage]));
-          mma_commit(smem_u32(&sm.tfull_bar[buf]));
+            mma_f8_elect(d, smem_desc_sw128(a0 + 32 * k), smem_desc_sw128(b0 + 32 * k), IDESC,
+                         k > 0 ? 1u : 0u);
+          mma_commit_elect(smem_u32(&sm.empty_bar[stage]));
+          mma_commit_elect(smem_u32(&sm.tfull_bar[buf]));
           if (++stage == STAGES) { stage = 0; phase ^= 1; }
         }
       }
       // all issued MMAs must finish before TMEM is released
-      mma_commit(smem_u32(&sm.drain_bar));
-      volatile int never = 0;
-      mbar_wait(smem_u32(&sm.drain_bar), 0, p.wait_limit, &never, p.status);
-    }
+      mma_commit_elect(smem_u32(&sm.drain_bar));
+      if (lane == 0) {
+        volatile int never = 0;
+        mbar_wait(smem_u32(&sm.drain_bar), 0, p.wait_limit, &never, p.status);
+      }
     }
   } else {
     // ------------------------------------------------ promotion + epilogue
