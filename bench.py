@@ -45,7 +45,11 @@ TRAFFIC_FILE = os.path.join(ROOT, "profiles", "gemm_fprop_traffic.json")
 def parse():
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
-    p.add_argument("--steps", type=int, default=2000)
+    p.add_argument("--steps", type=int, default=None,
+                   help="timed steps (default: 2000 for fprop, 200 for the other workloads)")
+    p.add_argument("--workload", choices=["fprop", "backward", "moe", "ksweep"], default="fprop",
+                   help="fprop is the headline step; the others time the remaining hot-path "
+                        "kernels on their own workloads (one JSON line each)")
     p.add_argument("--warmup", type=int, default=10)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--e2e-steps", type=int, default=20)
@@ -310,6 +314,235 @@ def run_ours(args, rank, world):
     return out
 
 
+# ---------------------------------------------------- other workloads
+def _timed_loop(ops, steps, warmup, stream, dev):
+    """Run `ops` (list of (name, fn)) back to back `steps` times after `warmup`
+    untimed steps; CUDA events around the whole region and around every op."""
+    import torch
+
+    for _ in range(max(warmup, 3)):
+        for _, fn in ops:
+            fn()
+    torch.cuda.synchronize()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(ops) + 1)]
+           for _ in range(steps)]
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    with ClockSampler(dev.index) as clk:
+        t0.record(stream)
+        for i in range(steps):
+            for j, (_, fn) in enumerate(ops):
+                evs[i][j].record(stream)
+                fn()
+            evs[i][len(ops)].record(stream)
+        t1.record(stream)
+        torch.cuda.synchronize()
+    per = {name: statistics.mean(e[j].elapsed_time(e[j + 1]) for e in evs)
+           for j, (name, _) in enumerate(ops)}
+    return t0.elapsed_time(t1), per, clk.summary()
+
+
+def run_workload(args, rank, world):
+    """Backward (Dgrad + Wgrad), routed-expert (grouped up and down) and K-sweep steps."""
+    import numpy as np
+    import torch
+
+    import fp8_fine_grained_19_b300 as fp8
+    import synth
+
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    lib = fp8.load()
+    stream = torch.cuda.current_stream()
+    sp = stream.cuda_stream
+    pk = peaks()
+    fp8_peak = 2.0 * pk["bf16_sustained"]
+    hbm = pk["hbm_gbs"]
+
+    def check(rc, what):
+        if rc != 0:
+            raise RuntimeError(f"{what}: {fp8.status_string(rc)}")
+
+    def u8(*shape):
+        return torch.empty(shape, dtype=torch.uint8, device=dev)
+
+    def f32(*shape):
+        return torch.empty(shape, dtype=torch.float32, device=dev)
+
+    # each op: (name, fn, kind, amount) with kind "hbm" (algorithmic bytes) or "tensor" (FLOPs)
+    ops = []
+    desc = {}
+    if args.workload == "backward":
+        Mt, Nf, Kh = 4096, 18432, 7168            # tokens, FFN width, hidden
+        case = synth.dense_case("fprop")
+        x = case.x().to(dev)
+        w = case.w().to(dev)
+        dy = synth.dy_bf16().to(dev)
+        qd, sd = u8(Mt, Nf), f32(Mt, Nf // 128)
+        qdt, sdt = u8(Nf, Mt), f32(Nf, Mt // 128)
+        qxt, sxt = u8(Kh, Mt), f32(Kh, Mt // 128)
+        qw, sw = u8(Nf, Kh), f32(Nf // 128, Kh // 128)
+        qwt, swt = u8(Kh, Nf), f32(Kh // 128, Nf // 128)
+        dx = torch.empty((Mt, Kh), dtype=torch.bfloat16, device=dev)
+        dw = torch.empty((Nf, Kh), dtype=torch.float32, device=dev)
+        qbytes = lambda r, c: r * c * 3 + r * c // 128 * 4  # noqa: E731
+        ops += [
+            ("act_quant_dY", lambda: check(lib.fp8_act_quant(dy.data_ptr(), fp8.BF16, Mt, Nf, qd.data_ptr(),
+                                                             sd.data_ptr(), 0, sp), "act_quant"),
+             "hbm", qbytes(Mt, Nf)),
+            ("act_quant_T_dY", lambda: check(lib.fp8_act_quant(dy.data_ptr(), fp8.BF16, Mt, Nf, qdt.data_ptr(),
+                                                               sdt.data_ptr(), fp8.TRANSPOSE, sp), "act_quant_T"),
+             "hbm", qbytes(Mt, Nf)),
+            ("act_quant_T_X", lambda: check(lib.fp8_act_quant(x.data_ptr(), fp8.BF16, Mt, Kh, qxt.data_ptr(),
+                                                              sxt.data_ptr(), fp8.TRANSPOSE, sp), "act_quant_T"),
+             "hbm", qbytes(Mt, Kh)),
+            ("weight_quant_W_with_T", lambda: check(lib.fp8_weight_quant(
+                w.data_ptr(), fp8.BF16, Nf, Kh, qw.data_ptr(), sw.data_ptr(), qwt.data_ptr(), swt.data_ptr(),
+                0, sp), "weight_quant"),
+             "hbm", Nf * Kh * 4 + 2 * (Nf // 128) * (Kh // 128) * 4),
+            ("gemm_dgrad", lambda: check(lib.fp8_blockscaled_gemm(
+                qd.data_ptr(), sd.data_ptr(), qwt.data_ptr(), swt.data_ptr(), dx.data_ptr(), fp8.BF16,
+                Mt, Kh, Nf, 0, sp), "dgrad"),
+             "tensor", 2 * Mt * Kh * Nf),
+            ("gemm_wgrad", lambda: check(lib.fp8_blockscaled_gemm(
+                qdt.data_ptr(), sdt.data_ptr(), qxt.data_ptr(), sxt.data_ptr(), dw.data_ptr(), fp8.F32,
+                Nf, Kh, Mt, fp8.B_TILE1x128, sp), "wgrad"),
+             "tensor", 2 * Nf * Kh * Mt),
+        ]
+        desc = {"workload": "backward_ffn_dy4096x18432_x4096x7168_w18432x7168",
+                "step": "act_quant dY (1x128) + 128x1 quant of dY and X + weight_quant W with W^T "
+                        "+ Dgrad dY.W -> bf16 [4096,7168] + Wgrad dY^T.X -> f32 [18432,7168]",
+                "data": "synthetic: dY N(0,1e-3^2), X N(0,1) 0.1% x100, W N(0,0.02^2)"}
+    elif args.workload == "moe":
+        case = synth.MOE_FULL
+        tok = case.tokens()
+        r = synth.moe_route(synth.bf16_to_f32(tok), case.router(), case.bias(), case.topk)
+        T, E, H, I = case.rows, case.E, case.H, case.I
+        tok = tok.to(dev)
+        off = torch.from_numpy(r["offsets"]).to(dev)
+        idx = torch.from_numpy(r["token_of_row"]).to(dev)
+        qu, su = u8(E, 2 * I, H), f32(E, 2 * I // 128, H // 128)
+        qdn, sdn = u8(E, H, I), f32(E, H // 128, I // 128)
+        for e in range(E):              # expert weights: drawn and quantised once (not timed)
+            q_e, s_e = fp8.weight_quant(synth.expert_weight(case, e, "up", dev))
+            qu[e].copy_(q_e)
+            su[e].copy_(s_e)
+            q_e, s_e = fp8.weight_quant(synth.expert_weight(case, e, "down", dev))
+            qdn[e].copy_(q_e)
+            sdn[e].copy_(s_e)
+        h = synth.swiglu_like_bf16((T, I), case.seed).to(dev)
+        qt, st = u8(case.T, H), f32(case.T, H // 128)
+        qh, sh = u8(T, I), f32(T, I // 128)
+        up = torch.empty((T, 2 * I), dtype=torch.bfloat16, device=dev)
+        down = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+        check(lib.fp8_act_quant(tok.data_ptr(), fp8.BF16, case.T, H, qt.data_ptr(), st.data_ptr(), fp8.POW2, sp),
+              "act_quant")
+        # dispatch (row gather in expert order) is routing glue: done once, outside the timed step
+        qa, sa = qt.index_select(0, idx).contiguous(), st.index_select(0, idx).contiguous()
+        torch.cuda.synchronize()
+        ops += [
+            ("act_quant_tokens_pow2", lambda: check(lib.fp8_act_quant(
+                tok.data_ptr(), fp8.BF16, case.T, H, qt.data_ptr(), st.data_ptr(), fp8.POW2, sp), "act_quant"),
+             "hbm", case.T * H * 3 + case.T * H // 128 * 4),
+            ("grouped_up", lambda: check(lib.fp8_grouped_gemm(
+                qa.data_ptr(), sa.data_ptr(), off.data_ptr(), E, T, qu.data_ptr(), su.data_ptr(), up.data_ptr(),
+                fp8.BF16, 2 * I, H, 0, sp), "grouped_up"),
+             "hbm", E * 2 * I * H + E * (2 * I // 128) * (H // 128) * 4 + T * H + T * H // 128 * 4 + T * 2 * I * 2),
+            ("act_quant_h_pow2", lambda: check(lib.fp8_act_quant(
+                h.data_ptr(), fp8.BF16, T, I, qh.data_ptr(), sh.data_ptr(), fp8.POW2, sp), "act_quant"),
+             "hbm", T * I * 3 + T * I // 128 * 4),
+            ("grouped_down", lambda: check(lib.fp8_grouped_gemm(
+                qh.data_ptr(), sh.data_ptr(), off.data_ptr(), E, T, qdn.data_ptr(), sdn.data_ptr(), down.data_ptr(),
+                fp8.BF16, H, I, 0, sp), "grouped_down"),
+             "hbm", E * H * I + E * (H // 128) * (I // 128) * 4 + T * I + T * I // 128 * 4 + T * H * 2),
+        ]
+        desc = {"workload": "moe_8192tok_h7168_e256_top8_inter2048",
+                "step": "act_quant tokens (pow2) + grouped up-proj [65536,7168]x[256,4096,7168] -> bf16 "
+                        "+ act_quant h (pow2) + grouped down-proj [65536,2048]x[256,7168,2048] -> bf16",
+                "routing": f"sigmoid + bias top-8 on the host; rows per expert {int(r['counts'].min())}.."
+                           f"{int(r['counts'].max())}; row gather done once outside the timed step",
+                "data": "synthetic: tokens N(0,1), router N(0,0.02^2), bias U(-0.1,0.1), experts N(0,0.02^2), "
+                        "h = silu(g)*u with g,u N(0,1.7^2)"}
+        flops = {"grouped_up": 2 * T * 2 * I * H, "grouped_down": 2 * T * H * I}
+    else:  # ksweep
+        for Kk in (4096, 8192, 16384):
+            cs = synth.dense_case(f"ksweep{Kk}")
+            xx, ww = cs.x().to(dev), cs.w().to(dev)
+            Mm, Nn = cs.M, cs.N
+            qa_, sa_ = u8(Mm, Kk), f32(Mm, Kk // 128)
+            qb_, sb_ = u8(Nn, Kk), f32(Nn // 128, Kk // 128)
+            cc = torch.empty((Mm, Nn), dtype=torch.float32, device=dev)
+
+            def mk(xx=xx, ww=ww, qa_=qa_, sa_=sa_, qb_=qb_, sb_=sb_, cc=cc, Mm=Mm, Nn=Nn, Kk=Kk):
+                return [
+                    (f"act_quant_k{Kk}", lambda: check(lib.fp8_act_quant(
+                        xx.data_ptr(), fp8.BF16, Mm, Kk, qa_.data_ptr(), sa_.data_ptr(), 0, sp), "act_quant"),
+                     "hbm", Mm * Kk * 3 + Mm * Kk // 128 * 4),
+                    (f"weight_quant_k{Kk}", lambda: check(lib.fp8_weight_quant(
+                        ww.data_ptr(), fp8.BF16, Nn, Kk, qb_.data_ptr(), sb_.data_ptr(), None, None, 0, sp),
+                        "weight_quant"),
+                     "hbm", Nn * Kk * 3 + (Nn // 128) * (Kk // 128) * 4),
+                    (f"gemm_k{Kk}", lambda: check(lib.fp8_blockscaled_gemm(
+                        qa_.data_ptr(), sa_.data_ptr(), qb_.data_ptr(), sb_.data_ptr(), cc.data_ptr(), fp8.F32,
+                        Mm, Nn, Kk, 0, sp), "gemm"),
+                     "tensor", 2 * Mm * Nn * Kk),
+                ]
+            ops += mk()
+        desc = {"workload": "ksweep_2048x2048_k4096_8192_16384",
+                "step": "per K: act_quant X + weight_quant W + gemm -> f32",
+                "data": "synthetic: X, W N(0,1) with 0.5% Student-t(2) replacements",
+                "l2": "working set 2-4x smaller than L2 for K <= 8192: these times include L2 hits"}
+
+    steps = args.steps
+    total_ms, per, clocks = _timed_loop([(n, f) for n, f, _, _ in ops], steps, args.warmup, stream, dev)
+    status = fp8.device_status()
+    if status != fp8.OK:
+        raise RuntimeError(f"device status {fp8.status_string(status)}")
+    gemm_flops = sum(a for _, _, k, a in ops if k == "tensor")
+    if args.workload == "moe":
+        gemm_flops = sum(flops.values())
+    per_op = {}
+    for name, _, kind, amount in ops:
+        ms = per[name]
+        if kind == "tensor":
+            tf = amount / (ms * 1e-3) / 1e12
+            per_op[name] = {"ms": round(ms, 5), "TFLOP/s": round(tf, 2),
+                            "frac_fp8_peak": round(tf / fp8_peak, 4)}
+        else:
+            gbs = amount / (ms * 1e-3) / 1e9
+            per_op[name] = {"ms": round(ms, 5), "GB/s": round(gbs, 1), "frac_hbm": round(gbs / hbm, 4),
+                            "bytes": amount}
+            if args.workload == "moe" and name in flops:
+                tf = flops[name] / (ms * 1e-3) / 1e12
+                t_mem = amount / (hbm * 1e9) * 1e3
+                t_tc = flops[name] / (fp8_peak * 1e12) * 1e3
+                per_op[name].update({"TFLOP/s": round(tf, 2), "roofline_ms": round(max(t_mem, t_tc), 5),
+                                     "frac_of_roofline": round(max(t_mem, t_tc) / ms, 4)})
+    dom = max(ops, key=lambda o: per[o[0]])
+    dname, _, dkind, damount = dom
+    if dkind == "tensor":
+        ach = damount / (per[dname] * 1e-3) / 1e12
+        roof = {"kernel": dname, "bound": "tensor", "achieved": round(ach, 2), "peak": round(fp8_peak, 1),
+                "unit": "TFLOP/s", "frac": round(ach / fp8_peak, 4),
+                "peak_source": f"2 x bf16 sustained, {pk['source']} ({pk['bf16_sustained']} TF/s)",
+                "traffic": None, "algorithmic_flops": damount}
+    else:
+        ach = damount / (per[dname] * 1e-3) / 1e9
+        roof = {"kernel": dname, "bound": "hbm", "achieved": round(ach, 1), "peak": hbm, "unit": "GB/s",
+                "frac": round(ach / hbm, 4), "peak_source": f"copy bandwidth, {pk['source']}",
+                "traffic": None, "algorithmic_bytes": damount}
+    cfg = dict(desc)
+    cfg["parallelism"] = f"{world} independent replica(s)"
+    return {
+        "metric": METRIC, "value": round(world * steps * gemm_flops / (total_ms * 1e-3) / 1e12, 3),
+        "unit": "TFLOP/s", "n_gpus": world, "steps": steps, "warmup": max(args.warmup, 3),
+        "ms_per_step": round(total_ms / steps, 5), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "e4m3 x e4m3 -> f32 accumulate", "data": "synthetic",
+        "config": cfg, "roofline": roof, "per_op": per_op, "e2e": None,
+        "gpu_launches": len(ops) * steps, "clocks": clocks,
+    }
+
+
 # ------------------------------------------------------------- CPU oracle
 def oracle_sample(rows_aq=2048, rows_wq=2048, rows_g=512, cols_g=4096, seed=0):
     """Time the oracle on a bounded sample of one step; extrapolate to the full step.
@@ -392,6 +625,8 @@ def run_reference(args):
 
 def main():
     args = parse()
+    if args.steps is None:
+        args.steps = 2000 if args.workload == "fprop" else 200
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     if args.impl == "reference":
@@ -402,6 +637,14 @@ def main():
         import torch
         torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
         torch.distributed.init_process_group("nccl")
+    if args.workload != "fprop":
+        out = run_workload(args, rank, world)
+        if rank == 0:
+            print(json.dumps(out), flush=True)
+        if world > 1:
+            import torch
+            torch.distributed.destroy_process_group()
+        return
     out = run_ours(args, rank, world)
     if rank == 0:
         if not args.no_cpu_baseline:

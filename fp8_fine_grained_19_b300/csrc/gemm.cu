@@ -31,6 +31,8 @@
 
 #include <cuda_bf16.h>
 
+#include <cstddef>
+
 #include "device_common.cuh"
 #include "launch.h"
 
@@ -56,6 +58,7 @@ static_assert(2 * REGS_EPILOGUE + REGS_PRODUCER <= 3 * REGS_LAUNCH, "register sp
 constexpr int TMEM_COLS = 512;
 constexpr int GROUP_M = 16;
 constexpr int MAX_EXPERTS = 1024;
+constexpr int SB_GROUP = 8;           // tile mode: slices whose B scales are shared per barrier
 constexpr uint32_t IDESC = idesc_e4m3_f32(BM, BN);
 
 struct GemmParams {
@@ -85,10 +88,14 @@ struct Smem {
   int abort_flag;
   int bad_offsets;
   int num_tiles;
-  float sbt[2][2][128];           // tile-mode B scales: [column half][slice counter parity][col]
+  // tile-mode B scales: [column half][group parity][slice][col]; read as float4
+  alignas(16) float sbt[2][2][SB_GROUP][128];
   int cum[MAX_EXPERTS + 1];       // grouped: tile prefix per expert
   int row0[MAX_EXPERTS + 1];      // grouped: copy of offsets
 };
+
+static_assert(offsetof(Smem, sbt) % 16 == 0, "float4 reads of the tile-mode scales");
+static_assert(offsetof(Smem, full_bar) % 8 == 0, "mbarriers are 8-byte aligned");
 
 struct Tile {
   int m0;       // first row of A / C
@@ -310,39 +317,93 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       // column) and are never stored
       const float* sa_row = p.sa + static_cast<int64_t>(row_ok ? row : 0) * nkb;
       const float* sb_ptr =
-          BTILE ? p.sb + static_cast<int64_t>(min(col_h + tid_h, p.N - 1)) * nkb
-                : p.sb + (static_cast<int64_t>(tl.e) * n_blocks + (half_ok ? col_h / 128 : 0)) * nkb;
+          p.sb + (static_cast<int64_t>(tl.e) * n_blocks + (half_ok ? col_h / 128 : 0)) * nkb;
 
       uint64_t acc[64];
 #pragma unroll
       for (int j = 0; j < 64; ++j) acc[j] = 0;
 
-      float sa_next = __ldg(sa_row);
-      float sb_next = __ldg(sb_ptr);
-      for (int kb = 0; kb < nkb; ++kb, ++it) {
-        const float sa_cur = sa_next, sb_cur = sb_next;
-        if (kb + 1 < nkb) {
-          sa_next = __ldg(sa_row + kb + 1);
-          sb_next = __ldg(sb_ptr + kb + 1);
-        }
-        const uint32_t buf = it & 1, bpar = (it >> 1) & 1;
-        const bool got =
-            mbar_wait(smem_u32(&sm.tfull_bar[buf]), bpar, p.wait_limit, abort_flag, p.status);
-        if constexpr (BTILE) {
-          // publish this slice's column scales to the half; the barrier also
-          // takes a vote so that all 128 threads leave together on an abort
-          sm.sbt[half][it & 1][tid_h] = sb_cur;
-          if (bar_any(1 + half, 128, !got)) {
-            ok = false;
-            break;
+      if constexpr (BTILE) {
+        // Column scales: thread tid_h owns column col_h + tid_h of its half and
+        // reads that column's scales SB_GROUP slices at a time (contiguous in
+        // sb).  The half shares them through a two-group ring in shared memory
+        // and synchronises once per group.  A thread whose wait gives up keeps
+        // walking the slices (without touching TMEM) so that every thread of
+        // the half passes the same barriers; the half then leaves together.
+        const float* sb_col = p.sb + static_cast<int64_t>(min(col_h + tid_h, p.N - 1)) * nkb;
+        float grp[SB_GROUP];
+#pragma unroll
+        for (int i = 0; i < SB_GROUP; ++i) grp[i] = i < nkb ? __ldg(sb_col + i) : 0.0f;
+#pragma unroll
+        for (int i = 0; i < SB_GROUP; ++i) sm.sbt[half][0][i][tid_h] = grp[i];
+#pragma unroll
+        for (int i = 0; i < SB_GROUP; ++i)
+          grp[i] = SB_GROUP + i < nkb ? __ldg(sb_col + SB_GROUP + i) : 0.0f;
+        bar_sync(1 + half, 128);
+        bool dead = false;
+        float sa_next = __ldg(sa_row);
+        for (int kb = 0; kb < nkb; ++kb, ++it) {
+          if (kb > 0 && kb % SB_GROUP == 0) {
+            const int g = kb / SB_GROUP;
+#pragma unroll
+            for (int i = 0; i < SB_GROUP; ++i) sm.sbt[half][g & 1][i][tid_h] = grp[i];
+#pragma unroll
+            for (int i = 0; i < SB_GROUP; ++i)
+              grp[i] = kb + SB_GROUP + i < nkb ? __ldg(sb_col + kb + SB_GROUP + i) : 0.0f;
+            bar_sync(1 + half, 128);
           }
-        } else if (!got) {
+          const float sa_cur = sa_next;
+          if (kb + 1 < nkb) sa_next = __ldg(sa_row + kb + 1);
+          const uint32_t buf = it & 1, bpar = (it >> 1) & 1;
+          if (!dead)
+            dead = !mbar_wait(smem_u32(&sm.tfull_bar[buf]), bpar, p.wait_limit, abort_flag, p.status);
+          if (dead) continue;
+          tc_fence_after();
+          const uint32_t taddr = lane_taddr + buf * BN;
+          const uint64_t sa2 = pack2(__float_as_uint(sa_cur), __float_as_uint(sa_cur));
+          const uint32_t sbv = smem_u32(&sm.sbt[half][(kb / SB_GROUP) & 1][kb % SB_GROUP][0]);
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            // the coefficients sa * sb[col] of this chunk are formed while its
+            // TMEM load is in flight; the scales are read as column pairs
+            uint32_t r[32];
+            tmem_ld_32cols(taddr + c * 32, r);
+            uint64_t cf[16];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              uint64_t q0, q1;
+              lds_2x64(sbv + (c * 32 + 4 * j) * 4, q0, q1);
+              cf[2 * j] = mul2(q0, sa2);
+              cf[2 * j + 1] = mul2(q1, sa2);
+            }
+            tmem_ld_wait();
+#pragma unroll
+            for (int j = 0; j < 16; ++j) fma2(acc[c * 16 + j], pack2(r[2 * j], r[2 * j + 1]), cf[j]);
+          }
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(smem_u32(&sm.tempty_bar[buf]));
+        }
+        if (bar_any(1 + half, 128, dead)) {
           ok = false;
           break;
         }
-        tc_fence_after();
-        const uint32_t taddr = lane_taddr + buf * BN;
-        if constexpr (!BTILE) {
+      } else {
+        float sa_next = __ldg(sa_row);
+        float sb_next = __ldg(sb_ptr);
+        for (int kb = 0; kb < nkb; ++kb, ++it) {
+          const float sa_cur = sa_next, sb_cur = sb_next;
+          if (kb + 1 < nkb) {
+            sa_next = __ldg(sa_row + kb + 1);
+            sb_next = __ldg(sb_ptr + kb + 1);
+          }
+          const uint32_t buf = it & 1, bpar = (it >> 1) & 1;
+          if (!mbar_wait(smem_u32(&sm.tfull_bar[buf]), bpar, p.wait_limit, abort_flag, p.status)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t taddr = lane_taddr + buf * BN;
           const float s = sa_cur * sb_cur;
           const uint64_t s2 = pack2(__float_as_uint(s), __float_as_uint(s));
 #pragma unroll
@@ -353,28 +414,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
             for (int j = 0; j < 16; ++j) fma2(acc[c * 16 + j], pack2(r[2 * j], r[2 * j + 1]), s2);
           }
-        } else {
-          const uint64_t sa2 = pack2(__float_as_uint(sa_cur), __float_as_uint(sa_cur));
-          const float* sbv = sm.sbt[half][it & 1];
-#pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            uint32_t r[32];
-            tmem_ld_32cols(taddr + c * 32, r);
-            tmem_ld_wait();
-#pragma unroll
-            for (int j = 0; j < 16; ++j) {
-              const float2 sbp = *reinterpret_cast<const float2*>(&sbv[c * 32 + 2 * j]);
-              const uint64_t coef =
-                  mul2(pack2(__float_as_uint(sbp.x), __float_as_uint(sbp.y)), sa2);
-              fma2(acc[c * 16 + j], pack2(r[2 * j], r[2 * j + 1]), coef);
-            }
-          }
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(smem_u32(&sm.tempty_bar[buf]));
         }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(&sm.tempty_bar[buf]));
+        if (!ok) break;
       }
-      if (!ok) break;
 
       // --- store this thread's row segment (128 columns of its half)
       if (row_ok && half_ok) {
