@@ -145,27 +145,32 @@ __global__ void __launch_bounds__(256) act_quant_rows_kernel(const T* __restrict
 
 // --------------------------------------------------------------------------
 // 128x1 tiles along M, transposed output.  One CTA owns rows [128 i, 128 i+128)
-// and columns [64 j, 64 j + 64) of x.  The block is staged as float in shared
-// memory; each column's amax comes from 4 quarter-column partials; then thread
-// (k, p) converts rows 32p..32p+31 of column k and writes 32 consecutive code
-// bytes of q^T row k (a full 32-byte sector).
+// and COLS columns of x (COLS = 128 for BF16, 64 for FP32: 32 KB either way),
+// staged raw in shared memory by coalesced 16-byte loads.  Thread (j, g) owns
+// the column pair (2j, 2j+1) and rows g*RPG.. of the block: it reads them as
+// 32- or 64-bit words (conflict-free), publishes its two partial amaxes, and
+// after one barrier reads them again, converts them and writes RPG code bytes
+// to each of q^T rows col0+2j and col0+2j+1.
 template <typename T>
 __global__ void __launch_bounds__(256) act_quant_cols_kernel(const T* __restrict__ x,
                                                              uint8_t* __restrict__ qt,
                                                              float* __restrict__ st, int M,
                                                              int K, int pow2) {
-  constexpr int ROWS = 128, COLS = 64;
+  constexpr int ROWS = 128;
+  constexpr int COLS = sizeof(T) == 2 ? 128 : 64;
   constexpr int EPV = Vec16<T>::N;            // elements per 16-byte vector
-  constexpr int VPR = COLS / EPV;             // vectors per tile row
-  __shared__ __align__(16) float tile[ROWS][COLS];
-  __shared__ float part[4][COLS];
-  __shared__ float mul[COLS];
+  constexpr int VPR = COLS / EPV;             // vectors per tile row (16)
+  constexpr int NV = ROWS * VPR / 256;        // vectors per thread (8)
+  constexpr int NPAIR = COLS / 2;             // column pairs
+  constexpr int RG = 256 / NPAIR;             // row groups (4 or 8)
+  constexpr int RPG = ROWS / RG;              // rows per group (32 or 16)
+  __shared__ __align__(16) T tile[ROWS][COLS];
+  __shared__ float part[RG][COLS];
 
   const int row0 = blockIdx.y * ROWS;
   const int col0 = blockIdx.x * COLS;
   const int t = threadIdx.x;
 
-  constexpr int NV = ROWS * VPR / 256;        // vectors per thread
   uint4 v[NV];
 #pragma unroll
   for (int i = 0; i < NV; ++i) {
@@ -177,47 +182,73 @@ __global__ void __launch_bounds__(256) act_quant_cols_kernel(const T* __restrict
   for (int i = 0; i < NV; ++i) {
     const int vid = t + 256 * i;
     const int r = vid / VPR, c = (vid % VPR) * EPV;
-    float f[EPV];
-    Vec16<T>::unpack(v[i], f);
-#pragma unroll
-    for (int e = 0; e < EPV; e += 4)
-      *reinterpret_cast<float4*>(&tile[r][c + e]) = make_float4(f[e], f[e + 1], f[e + 2], f[e + 3]);
+    *reinterpret_cast<uint4*>(&tile[r][c]) = v[i];
   }
   __syncthreads();
 
-  const int k = t % COLS, p = t / COLS;       // column, quarter (32 rows)
-  float amax = 0.0f;
-#pragma unroll 8
-  for (int j = 0; j < 32; ++j) amax = fmaxf(amax, fabsf(tile[32 * p + j][k]));
-  part[p][k] = amax;
-  __syncthreads();
-  if (t < COLS) {
-    const float a = fmaxf(fmaxf(part[0][t], part[1][t]), fmaxf(part[2][t], part[3][t]));
-    const Scale sc = scale_from_amax(a, pow2 != 0);
-    mul[t] = sc.m;
-    st[static_cast<int64_t>(col0 + t) * (M / ROWS) + blockIdx.y] = sc.s;
-  }
-  __syncthreads();
-
-  const float m = mul[k];
-  uint32_t w[8];
+  const int j = t % NPAIR, g = t / NPAIR;
+  // the column pair (2j, 2j+1) at row r of this thread's group
+  auto pair_at = [&](int r, float& x0, float& x1) {
+    if constexpr (sizeof(T) == 2) {
+      const uint32_t w = *reinterpret_cast<const uint32_t*>(&tile[g * RPG + r][2 * j]);
+      x0 = __uint_as_float(w << 16);
+      x1 = __uint_as_float(w & 0xFFFF0000u);
+    } else {
+      const float2 w = *reinterpret_cast<const float2*>(&tile[g * RPG + r][2 * j]);
+      x0 = w.x;
+      x1 = w.y;
+    }
+  };
+  float a0 = 0.0f, a1 = 0.0f;
 #pragma unroll
-  for (int j = 0; j < 8; ++j) {
-    const float* r4 = &tile[32 * p + 4 * j][k];
-    const uint32_t lo = e4m3x2(__fmul_rn(r4[0], m), __fmul_rn(r4[COLS], m));
-    const uint32_t hi = e4m3x2(__fmul_rn(r4[2 * COLS], m), __fmul_rn(r4[3 * COLS], m));
-    w[j] = lo | (hi << 16);
+  for (int r = 0; r < RPG; ++r) {
+    float x0, x1;
+    pair_at(r, x0, x1);
+    a0 = fmaxf(a0, fabsf(x0));
+    a1 = fmaxf(a1, fabsf(x1));
   }
-  uint4* dst = reinterpret_cast<uint4*>(qt + static_cast<int64_t>(col0 + k) * M + row0 + 32 * p);
-  dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
-  dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+  part[g][2 * j] = a0;
+  part[g][2 * j + 1] = a1;
+  __syncthreads();
+#pragma unroll
+  for (int i = 0; i < RG; ++i) {
+    a0 = fmaxf(a0, part[i][2 * j]);
+    a1 = fmaxf(a1, part[i][2 * j + 1]);
+  }
+  const Scale s0 = scale_from_amax(a0, pow2 != 0);
+  const Scale s1 = scale_from_amax(a1, pow2 != 0);
+  if (g == 0) {
+    st[static_cast<int64_t>(col0 + 2 * j) * (M / ROWS) + blockIdx.y] = s0.s;
+    st[static_cast<int64_t>(col0 + 2 * j + 1) * (M / ROWS) + blockIdx.y] = s1.s;
+  }
+  // second pass over the same shared words (cheaper than holding 2 x RPG
+  // values in registers, which would cap the CTAs per SM)
+  uint32_t w0[RPG / 4], w1[RPG / 4];
+#pragma unroll
+  for (int i = 0; i < RPG / 4; ++i) {
+    float x[4], y[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) pair_at(4 * i + e, x[e], y[e]);
+    w0[i] = e4m3x2(__fmul_rn(x[0], s0.m), __fmul_rn(x[1], s0.m)) |
+            (e4m3x2(__fmul_rn(x[2], s0.m), __fmul_rn(x[3], s0.m)) << 16);
+    w1[i] = e4m3x2(__fmul_rn(y[0], s1.m), __fmul_rn(y[1], s1.m)) |
+            (e4m3x2(__fmul_rn(y[2], s1.m), __fmul_rn(y[3], s1.m)) << 16);
+  }
+  uint4* d0 = reinterpret_cast<uint4*>(qt + static_cast<int64_t>(col0 + 2 * j) * M + row0 + g * RPG);
+  uint4* d1 = reinterpret_cast<uint4*>(qt + static_cast<int64_t>(col0 + 2 * j + 1) * M + row0 + g * RPG);
+#pragma unroll
+  for (int i = 0; i < RPG / 16; ++i) {
+    d0[i] = make_uint4(w0[4 * i], w0[4 * i + 1], w0[4 * i + 2], w0[4 * i + 3]);
+    d1[i] = make_uint4(w1[4 * i], w1[4 * i + 1], w1[4 * i + 2], w1[4 * i + 3]);
+  }
 }
 
 // --------------------------------------------------------------------------
 // 128x128 blocks.  One CTA per block: stage the block (input type) in shared
 // memory while reducing the amax, then write row-major codes (8 bytes per
-// lane, coalesced) and, if requested, the transposed codes (thread (k, p)
-// walks rows 64p..64p+63 of column k and writes 64 bytes of q^T row k).
+// lane, coalesced) and, if requested, the transposed codes (thread (j, g)
+// reads columns 2j, 2j+1 of rows 32g..32g+31 and writes 32 bytes of each of
+// q^T rows 2j and 2j+1).
 template <typename T>
 __global__ void __launch_bounds__(256) weight_quant_kernel(const T* __restrict__ w,
                                                            uint8_t* __restrict__ q,
@@ -291,20 +322,38 @@ __global__ void __launch_bounds__(256) weight_quant_kernel(const T* __restrict__
   }
 
   if (qt != nullptr) {
-    const int k = t % B, p = t / B;           // column of the block, half (64 rows)
-    uint32_t wv[16];
+    // thread (j, g): columns 2j, 2j+1 of the block, rows 32g..32g+31, read as
+    // one 32- or 64-bit shared word per row (conflict-free)
+    const int j = t % 64, g = t / 64;
+    uint32_t w0[8], w1[8];
 #pragma unroll
-    for (int j = 0; j < 16; ++j) {
-      const int r = 64 * p + 4 * j;
-      const uint32_t lo = e4m3x2(__fmul_rn(to_f32(blk[r][k]), sc.m),
-                                 __fmul_rn(to_f32(blk[r + 1][k]), sc.m));
-      const uint32_t hi = e4m3x2(__fmul_rn(to_f32(blk[r + 2][k]), sc.m),
-                                 __fmul_rn(to_f32(blk[r + 3][k]), sc.m));
-      wv[j] = lo | (hi << 16);
+    for (int i = 0; i < 8; ++i) {
+      float x[4], y[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int r = 32 * g + 4 * i + e;
+        if constexpr (sizeof(T) == 2) {
+          const uint32_t w = *reinterpret_cast<const uint32_t*>(&blk[r][2 * j]);
+          x[e] = __uint_as_float(w << 16);
+          y[e] = __uint_as_float(w & 0xFFFF0000u);
+        } else {
+          const float2 w = *reinterpret_cast<const float2*>(&blk[r][2 * j]);
+          x[e] = w.x;
+          y[e] = w.y;
+        }
+      }
+      w0[i] = e4m3x2(__fmul_rn(x[0], sc.m), __fmul_rn(x[1], sc.m)) |
+              (e4m3x2(__fmul_rn(x[2], sc.m), __fmul_rn(x[3], sc.m)) << 16);
+      w1[i] = e4m3x2(__fmul_rn(y[0], sc.m), __fmul_rn(y[1], sc.m)) |
+              (e4m3x2(__fmul_rn(y[2], sc.m), __fmul_rn(y[3], sc.m)) << 16);
     }
-    uint4* dst = reinterpret_cast<uint4*>(qt + static_cast<int64_t>(col0 + k) * N + row0 + 64 * p);
-#pragma unroll
-    for (int j = 0; j < 4; ++j) dst[j] = make_uint4(wv[4 * j], wv[4 * j + 1], wv[4 * j + 2], wv[4 * j + 3]);
+    uint4* d0 = reinterpret_cast<uint4*>(qt + static_cast<int64_t>(col0 + 2 * j) * N + row0 + 32 * g);
+    uint4* d1 =
+        reinterpret_cast<uint4*>(qt + static_cast<int64_t>(col0 + 2 * j + 1) * N + row0 + 32 * g);
+    d0[0] = make_uint4(w0[0], w0[1], w0[2], w0[3]);
+    d0[1] = make_uint4(w0[4], w0[5], w0[6], w0[7]);
+    d1[0] = make_uint4(w1[0], w1[1], w1[2], w1[3]);
+    d1[1] = make_uint4(w1[4], w1[5], w1[6], w1[7]);
   }
 }
 
@@ -331,7 +380,8 @@ cudaError_t launch_act_quant_rows(const void* x, fp8fg_dtype xt, int64_t M, int6
 
 cudaError_t launch_act_quant_cols(const void* x, fp8fg_dtype xt, int64_t M, int64_t K, uint8_t* qt,
                                   float* st_, bool pow2, cudaStream_t st) {
-  const dim3 grid(static_cast<unsigned>(K / 64), static_cast<unsigned>(M / 128));
+  const unsigned cols = xt == FP8FG_BF16 ? 128 : 64;    // columns per CTA (K % 128 == 0)
+  const dim3 grid(static_cast<unsigned>(K / cols), static_cast<unsigned>(M / 128));
   if (xt == FP8FG_BF16)
     act_quant_cols_kernel<__nv_bfloat16><<<grid, 256, 0, st>>>(
         static_cast<const __nv_bfloat16*>(x), qt, st_, static_cast<int>(M), static_cast<int>(K),

@@ -13,7 +13,9 @@ Pins (checked in tests/test_oracle_*.py without a GPU):
          casts (ml_dtypes, torch); saturation.
   quant  amax maps to +-448 exactly; power-of-2 scale rule; error bound of
          one E4M3 half-ulp times the tile amax; a hand-worked tile fixture;
-         transposed mode equals quantising the transpose.
+         transposed mode equals quantising the transpose; backward
+         re-quantisation of stored codes against a hand-worked block and a
+         two-step error bound.
   gemm   brute force in exact rationals on tiny shapes; int64 per-slice sums;
          special cases that reduce to a library matmul; scale linearity;
          Dgrad/Wgrad transposition identities.
@@ -23,6 +25,6 @@ figure (no mechanism detail to reproduce it); it is context only.
 """
 
 from .e4m3 import E4M3_MAX, decode, encode  # noqa: F401
-from .quant import (act_quant, act_quant_t, weight_quant, dequant_tiles,  # noqa: F401
-                    dequant_blocks, scale_from_amax)
+from .quant import (act_quant, act_quant_t, weight_quant, requant_t,  # noqa: F401
+                    dequant_tiles, dequant_blocks, scale_from_amax)
 from .scaled_gemm import gemm, grouped_gemm, slice_partials  # noqa: F401

@@ -100,6 +100,28 @@ def weight_quant(w, pow2: bool = False, transposed: bool = False):
     return q, s, np.ascontiguousarray(q.T), np.ascontiguousarray(s.T)
 
 
+def requant_t(q, s, pow2: bool = False):
+    """Backward re-quantisation of stored 1x128 codes into transposed 128x1 tiles.
+
+    Page 5 (inprokorea.com free #890463), backward-pass passage: the FP8
+    activations kept from the forward pass are read, dequantised, transposed
+    and quantised again in 128x1 tiles for the weight gradient.
+    q: uint8 [M, K] E4M3 codes with 1x128 scales s: float32 [M, K/128] (the
+    layout act_quant produces); M % 128 == 0.  Each element is dequantised in
+    float32 with one IEEE multiply, x = fl32(decode(q[r, k]) * s[r, k // 128])
+    (E4M3 values are exact in float32), and x is then quantised exactly as
+    act_quant_t.  Returns (qt uint8 [K, M], st float32 [K, M/128]).
+    """
+    q = np.asarray(q)
+    M, K = q.shape
+    if K % TILE or M % TILE:
+        raise ValueError("M and K must be multiples of 128")
+    v = decode(q).astype(np.float32)
+    sc = np.repeat(np.asarray(s, dtype=np.float32), TILE, axis=1)[:, :K]
+    x = (v * sc).astype(np.float32)                  # one IEEE float32 multiply
+    return act_quant_t(x, pow2=pow2)
+
+
 def dequant_tiles(q, s) -> np.ndarray:
     """Inverse of act_quant (float64): x_hat[r, k] = decode(q[r, k]) * s[r, k // 128]."""
     v = decode(q)

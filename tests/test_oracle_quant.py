@@ -209,3 +209,76 @@ def test_planted_mistakes_are_caught(monkeypatch):
     monkeypatch.setattr(oq, "scale_from_amax", lambda a, pow2=False: pow2_round_down(a) if pow2 else real(a))
     with pytest.raises(AssertionError):
         test_pow2_rule()
+
+
+# ---------------------------------------------------------------- backward re-quantisation
+REQUANT_GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "requant_t_worked.txt")
+
+
+def _requant_fixture_input():
+    q = np.empty((128, 256), np.uint8)
+    q[:, :128] = 0x38
+    q[:, 128::2] = 0x3C
+    q[:, 129::2] = 0xBC
+    s = np.empty((128, 2), np.float32)
+    s[:, 0] = 2.0 ** (np.arange(128) % 8)
+    s[:, 1] = 0.25
+    return q, s
+
+
+def test_requant_worked_block():
+    q, s = _requant_fixture_input()
+    scales, codes = {}, {}
+    for line in open(REQUANT_GOLDEN):
+        f = line.split("#")[0].split()
+        if not f:
+            continue
+        if f[0] == "scale":
+            scales[(f[1], int(f[2]))] = int(f[3], 16)
+        else:
+            codes[(f[1], int(f[2]), int(f[3]))] = int(f[4], 16)
+    for mode in ("default", "pow2"):
+        qt, st = oracle.requant_t(q, s, pow2=(mode == "pow2"))
+        assert qt.shape == (256, 128) and st.shape == (256, 1)
+        stb = st.view(np.uint32)
+        assert (stb[:128, 0] == scales[(mode, 0)]).all()
+        assert (stb[128:, 0] == scales[(mode, 1)]).all()
+        for r in range(128):
+            assert (qt[:128, r] == codes[(mode, 0, r % 8)]).all(), (mode, r)
+        assert (qt[128::2, :] == codes[(mode, 1, 0)]).all()
+        assert (qt[129::2, :] == codes[(mode, 1, 1)]).all()
+
+
+@pytest.mark.parametrize("pow2", [False, True])
+def test_requant_two_step_error_bound(pow2):
+    # quantise 1x128, then re-quantise 128x1: each step is within half an E4M3
+    # step of its input (relative 2^-4 for normal codes, 2^-10 * s below 2^-6),
+    # so the composition is within the sum of the two bounds
+    x = _rand((256, 384), 21, heavy=False)
+    q, s = oracle.act_quant(x)
+    qt, st = oracle.requant_t(q, s, pow2=pow2)
+    x1 = oracle.dequant_tiles(q, s)                       # after the first step
+    x2 = (e4m3.decode(qt) * np.repeat(st.astype(np.float64), 128, axis=1)).T
+    s1 = np.repeat(s.astype(np.float64), 128, axis=1)
+    s2 = np.repeat(st.astype(np.float64), 128, axis=1).T
+    b1 = np.maximum(2.0 ** -4 * np.abs(x), 2.0 ** -10 * s1) * (1 + 2.0 ** -20)
+    b2 = np.maximum(2.0 ** -4 * np.abs(x1), 2.0 ** -10 * s2) * (1 + 2.0 ** -20)
+    assert (np.abs(x2 - x) <= b1 + b2).all()
+
+
+def test_requant_uses_the_right_row_scale():
+    # every row has its own scale: a transposed or shared scale index would
+    # give a different column amax and different codes
+    g = np.random.default_rng(4)
+    q = e4m3.encode(g.standard_normal((256, 128)).astype(np.float32) * 40)
+    s = np.exp(g.uniform(-5, 5, (256, 1))).astype(np.float32)
+    qt, st = oracle.requant_t(q, s)
+    x = (e4m3.decode(q) * s.astype(np.float64)).astype(np.float32)
+    # the 128x1 tile amax of column k over rows 0..127 is max_r |x[r, k]|
+    amax = np.max(np.abs(x[:128]), axis=0).astype(np.float32)
+    assert np.array_equal(st[:, 0], (amax / np.float32(448)).astype(np.float32))
+
+
+def test_requant_rejects_ragged_rows():
+    with pytest.raises(ValueError):
+        oracle.requant_t(np.zeros((100, 128), np.uint8), np.ones((100, 1), np.float32))
