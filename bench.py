@@ -384,6 +384,9 @@ def run_workload(args, rank, world):
         qw, sw = u8(Nf, Kh), f32(Nf // 128, Kh // 128)
         qwt, swt = u8(Kh, Nf), f32(Kh // 128, Nf // 128)
         dx = torch.empty((Mt, Kh), dtype=torch.bfloat16, device=dev)
+        # X as the forward pass stored it: E4M3 codes with 1x128 scales
+        qx, sx = u8(Mt, Kh), f32(Mt, Kh // 128)
+        check(lib.fp8_act_quant(x.data_ptr(), fp8.BF16, Mt, Kh, qx.data_ptr(), sx.data_ptr(), 0, sp), "act_quant")
         dw = torch.empty((Nf, Kh), dtype=torch.float32, device=dev)
         qbytes = lambda r, c: r * c * 3 + r * c // 128 * 4  # noqa: E731
         ops += [
@@ -393,9 +396,9 @@ def run_workload(args, rank, world):
             ("act_quant_T_dY", lambda: check(lib.fp8_act_quant(dy.data_ptr(), fp8.BF16, Mt, Nf, qdt.data_ptr(),
                                                                sdt.data_ptr(), fp8.TRANSPOSE, sp), "act_quant_T"),
              "hbm", qbytes(Mt, Nf)),
-            ("act_quant_T_X", lambda: check(lib.fp8_act_quant(x.data_ptr(), fp8.BF16, Mt, Kh, qxt.data_ptr(),
-                                                              sxt.data_ptr(), fp8.TRANSPOSE, sp), "act_quant_T"),
-             "hbm", qbytes(Mt, Kh)),
+            ("requant_T_X_stored", lambda: check(lib.fp8_requant_transpose(
+                qx.data_ptr(), sx.data_ptr(), Mt, Kh, qxt.data_ptr(), sxt.data_ptr(), 0, sp), "requant_T"),
+             "hbm", Mt * Kh * 2 + Mt * (Kh // 128) * 4 + Kh * (Mt // 128) * 4),
             ("weight_quant_W_with_T", lambda: check(lib.fp8_weight_quant(
                 w.data_ptr(), fp8.BF16, Nf, Kh, qw.data_ptr(), sw.data_ptr(), qwt.data_ptr(), swt.data_ptr(),
                 0, sp), "weight_quant"),
@@ -410,8 +413,9 @@ def run_workload(args, rank, world):
              "tensor", 2 * Nf * Kh * Mt),
         ]
         desc = {"workload": "backward_ffn_dy4096x18432_x4096x7168_w18432x7168",
-                "step": "act_quant dY (1x128) + 128x1 quant of dY and X + weight_quant W with W^T "
-                        "+ Dgrad dY.W -> bf16 [4096,7168] + Wgrad dY^T.X -> f32 [18432,7168]",
+                "step": "act_quant dY (1x128) + 128x1 quant of dY + 128x1 re-quantisation of the stored "
+                        "FP8 X + weight_quant W with W^T + Dgrad dY.W -> bf16 [4096,7168] "
+                        "+ Wgrad dY^T.X -> f32 [18432,7168]",
                 "data": "synthetic: dY N(0,1e-3^2), X N(0,1) 0.1% x100, W N(0,0.02^2)"}
     elif args.workload == "moe":
         case = synth.MOE_FULL

@@ -16,7 +16,8 @@ import os
 import torch
 
 __all__ = [
-    "Fp8Error", "load", "lib_path", "act_quant", "weight_quant", "gemm", "grouped_gemm",
+    "Fp8Error", "load", "lib_path", "act_quant", "weight_quant", "requant_transpose", "gemm",
+    "grouped_gemm",
     "device_status", "set_wait_limit", "selftest_wait_timeout", "status_string",
     "OK", "ERR_INVALID_ARG", "ERR_UNSUPPORTED_SHAPE", "ERR_MISALIGNED", "ERR_CUDA",
     "ERR_TIMEOUT", "ERR_BAD_OFFSETS", "POW2", "TRANSPOSE", "B_TILE1x128", "BF16", "F32",
@@ -34,6 +35,7 @@ _vp, _i64, _u32, _i32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_uint, ctypes.c
 _SIGS = {
     "fp8_act_quant": [_vp, ctypes.c_int, _i64, _i64, _vp, _vp, _u32, _vp],
     "fp8_weight_quant": [_vp, ctypes.c_int, _i64, _i64, _vp, _vp, _vp, _vp, _u32, _vp],
+    "fp8_requant_transpose": [_vp, _vp, _i64, _i64, _vp, _vp, _u32, _vp],
     "fp8_blockscaled_gemm": [_vp, _vp, _vp, _vp, _vp, ctypes.c_int, _i64, _i64, _i64, _u32, _vp],
     "fp8_grouped_gemm": [_vp, _vp, _vp, _i32, _i64, _vp, _vp, _vp, ctypes.c_int, _i64, _i64,
                          _u32, _vp],
@@ -140,6 +142,19 @@ def weight_quant(w: torch.Tensor, pow2: bool = False, transposed: bool = False, 
                                    _ptr(st), POW2 if pow2 else 0, _stream(stream)),
            "fp8_weight_quant")
     return (q, s, qt, st) if transposed else (q, s)
+
+
+def requant_transpose(q: torch.Tensor, s: torch.Tensor, pow2: bool = False, stream=None):
+    """Stored 1x128 codes (q [M, K], s [M, K/128]) -> 128x1 tiles (q_t [K, M], s_t [K, M/128])."""
+    _need(q, (torch.uint8,), "q")
+    _need(s, (torch.float32,), "s")
+    M, K = q.shape
+    qt = torch.empty((K, M), dtype=torch.uint8, device=q.device)
+    st = torch.empty((K, M // 128 if M % 128 == 0 else 1), dtype=torch.float32, device=q.device)
+    _check(load().fp8_requant_transpose(_ptr(q), _ptr(s), M, K, _ptr(qt), _ptr(st),
+                                        POW2 if pow2 else 0, _stream(stream)),
+           "fp8_requant_transpose")
+    return qt, st
 
 
 def _out_code(dtype) -> int:

@@ -127,7 +127,7 @@ bool have_device() { return device_sm_count() > 0; }
 
 extern "C" {
 
-int fp8fg_abi_version(void) { return 1; }
+int fp8fg_abi_version(void) { return 2; }
 
 const char* fp8fg_status_string(fp8fg_status status) {
   switch (status) {
@@ -158,6 +158,22 @@ fp8fg_status fp8_act_quant(const void* x, fp8fg_dtype x_dtype, int64_t M, int64_
   const bool pow2 = (flags & FP8FG_POW2) != 0;
   if (trans) return from_cuda(launch_act_quant_cols(x, x_dtype, M, K, q, s, pow2, as_stream(stream)));
   return from_cuda(launch_act_quant_rows(x, x_dtype, M, K, q, s, pow2, as_stream(stream)));
+}
+
+fp8fg_status fp8_requant_transpose(const uint8_t* q, const float* s, int64_t M, int64_t K,
+                                   uint8_t* q_t, float* s_t, unsigned flags, void* stream) {
+  if ((flags & ~FP8FG_POW2) != 0 || M < 0 || K < 0) return FP8FG_ERR_INVALID_ARG;
+  if (M > 0 && (q == nullptr || s == nullptr || q_t == nullptr || s_t == nullptr))
+    return FP8FG_ERR_INVALID_ARG;
+  if (K < 128 || K % 128 != 0 || M % 128 != 0 || M > kMaxDim || K > kMaxDim ||
+      M / 128 > 65535)
+    return FP8FG_ERR_UNSUPPORTED_SHAPE;
+  if (!aligned16(q) || !aligned16(s) || !aligned16(q_t) || !aligned16(s_t))
+    return FP8FG_ERR_MISALIGNED;
+  if (M == 0) return FP8FG_OK;
+  if (!have_device()) return FP8FG_ERR_CUDA;
+  return from_cuda(launch_requant_t(q, s, M, K, q_t, s_t, (flags & FP8FG_POW2) != 0,
+                                    as_stream(stream)));
 }
 
 fp8fg_status fp8_weight_quant(const void* w, fp8fg_dtype w_dtype, int64_t N, int64_t K, uint8_t* q,

@@ -20,6 +20,8 @@ cudaError_t launch_act_quant_rows(const void* x, fp8fg_dtype xt, int64_t M, int6
                                   float* s, bool pow2, cudaStream_t st);
 cudaError_t launch_act_quant_cols(const void* x, fp8fg_dtype xt, int64_t M, int64_t K, uint8_t* qt,
                                   float* st_, bool pow2, cudaStream_t st);
+cudaError_t launch_requant_t(const uint8_t* q, const float* s, int64_t M, int64_t K, uint8_t* qt,
+                             float* st_, bool pow2, cudaStream_t st);
 cudaError_t launch_weight_quant(const void* w, fp8fg_dtype wt, int64_t N, int64_t K, uint8_t* q,
                                 float* s, uint8_t* qt, float* st_, bool pow2, cudaStream_t st);
 

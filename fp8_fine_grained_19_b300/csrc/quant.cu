@@ -16,6 +16,7 @@
 // packed e4m3x2 conversion, and grids sized in multiples of the SM count.
 
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 
 #include "device_common.cuh"
 #include "launch.h"
@@ -244,6 +245,102 @@ __global__ void __launch_bounds__(256) act_quant_cols_kernel(const T* __restrict
 }
 
 // --------------------------------------------------------------------------
+// Backward re-quantisation (page 5, backward-pass passage): stored E4M3 codes
+// with 1x128 scales -> dequantise (one FP32 multiply) -> 128x1 tiles with
+// transposed output.  One CTA owns rows [128 i, 128 i+128) and the 128 columns
+// of one scale group, so each row has a single scale: the 16 KB code block and
+// the 128 row scales are staged in shared memory.  Thread (j, g) owns the
+// column pair (2j, 2j+1) and rows 32g..32g+31; as in act_quant_cols it takes
+// the column amax in a first pass and converts in a second, writing 32 code
+// bytes to each of q^T rows col0+2j and col0+2j+1.
+__device__ __forceinline__ void e4m3x2_to_f32(uint32_t two_codes, float& lo, float& hi) {
+  uint32_t h2;   // E4M3 -> FP16 is exact (E4M3 is a subset of FP16)
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(static_cast<uint16_t>(two_codes)));
+  lo = __half2float(__ushort_as_half(static_cast<unsigned short>(h2 & 0xFFFFu)));
+  hi = __half2float(__ushort_as_half(static_cast<unsigned short>(h2 >> 16)));
+}
+
+__global__ void __launch_bounds__(256) requant_t_kernel(const uint8_t* __restrict__ q,
+                                                        const float* __restrict__ s,
+                                                        uint8_t* __restrict__ qt,
+                                                        float* __restrict__ st, int M, int K,
+                                                        int pow2) {
+  constexpr int ROWS = 128, COLS = 128, RPG = 32;
+  __shared__ __align__(16) uint8_t tile[ROWS][COLS];
+  __shared__ float rs[ROWS];
+  __shared__ float part[4][COLS];
+  const int row0 = blockIdx.y * ROWS;
+  const int col0 = blockIdx.x * COLS;
+  const int nkg = K / 128;
+  const int t = threadIdx.x;
+
+  uint4 v[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int vid = t + 256 * i;
+    const int r = vid / 8, c = (vid % 8) * 16;
+    v[i] = ld_stream16(q + static_cast<int64_t>(row0 + r) * K + col0 + c);
+  }
+  if (t < ROWS) rs[t] = __ldg(s + static_cast<int64_t>(row0 + t) * nkg + blockIdx.x);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int vid = t + 256 * i;
+    *reinterpret_cast<uint4*>(&tile[vid / 8][(vid % 8) * 16]) = v[i];
+  }
+  __syncthreads();
+
+  const int j = t % 64, g = t / 64;
+  auto pair_at = [&](int r, float& x0, float& x1) {
+    const int row = g * RPG + r;
+    const uint32_t two = *reinterpret_cast<const uint16_t*>(&tile[row][2 * j]);
+    float d0, d1;
+    e4m3x2_to_f32(two, d0, d1);
+    const float sc = rs[row];
+    x0 = __fmul_rn(d0, sc);
+    x1 = __fmul_rn(d1, sc);
+  };
+  float a0 = 0.0f, a1 = 0.0f;
+#pragma unroll 8
+  for (int r = 0; r < RPG; ++r) {
+    float x0, x1;
+    pair_at(r, x0, x1);
+    a0 = fmaxf(a0, fabsf(x0));
+    a1 = fmaxf(a1, fabsf(x1));
+  }
+  part[g][2 * j] = a0;
+  part[g][2 * j + 1] = a1;
+  __syncthreads();
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    a0 = fmaxf(a0, part[i][2 * j]);
+    a1 = fmaxf(a1, part[i][2 * j + 1]);
+  }
+  const Scale s0 = scale_from_amax(a0, pow2 != 0);
+  const Scale s1 = scale_from_amax(a1, pow2 != 0);
+  if (g == 0) {
+    st[static_cast<int64_t>(col0 + 2 * j) * (M / ROWS) + blockIdx.y] = s0.s;
+    st[static_cast<int64_t>(col0 + 2 * j + 1) * (M / ROWS) + blockIdx.y] = s1.s;
+  }
+  uint32_t w0[RPG / 4], w1[RPG / 4];
+#pragma unroll
+  for (int i = 0; i < RPG / 4; ++i) {
+    float x[4], y[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) pair_at(4 * i + e, x[e], y[e]);
+    w0[i] = e4m3x2(__fmul_rn(x[0], s0.m), __fmul_rn(x[1], s0.m)) |
+            (e4m3x2(__fmul_rn(x[2], s0.m), __fmul_rn(x[3], s0.m)) << 16);
+    w1[i] = e4m3x2(__fmul_rn(y[0], s1.m), __fmul_rn(y[1], s1.m)) |
+            (e4m3x2(__fmul_rn(y[2], s1.m), __fmul_rn(y[3], s1.m)) << 16);
+  }
+  uint4* d0 = reinterpret_cast<uint4*>(qt + static_cast<int64_t>(col0 + 2 * j) * M + row0 + g * RPG);
+  uint4* d1 = reinterpret_cast<uint4*>(qt + static_cast<int64_t>(col0 + 2 * j + 1) * M + row0 + g * RPG);
+  d0[0] = make_uint4(w0[0], w0[1], w0[2], w0[3]);
+  d0[1] = make_uint4(w0[4], w0[5], w0[6], w0[7]);
+  d1[0] = make_uint4(w1[0], w1[1], w1[2], w1[3]);
+  d1[1] = make_uint4(w1[4], w1[5], w1[6], w1[7]);
+}
+
+// --------------------------------------------------------------------------
 // 128x128 blocks.  One CTA per block: stage the block (input type) in shared
 // memory while reducing the amax, then write row-major codes (8 bytes per
 // lane, coalesced) and, if requested, the transposed codes (thread (j, g)
@@ -390,6 +487,14 @@ cudaError_t launch_act_quant_cols(const void* x, fp8fg_dtype xt, int64_t M, int6
     act_quant_cols_kernel<float><<<grid, 256, 0, st>>>(static_cast<const float*>(x), qt, st_,
                                                        static_cast<int>(M), static_cast<int>(K),
                                                        pow2 ? 1 : 0);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_requant_t(const uint8_t* q, const float* s, int64_t M, int64_t K, uint8_t* qt,
+                             float* st_, bool pow2, cudaStream_t st) {
+  const dim3 grid(static_cast<unsigned>(K / 128), static_cast<unsigned>(M / 128));
+  requant_t_kernel<<<grid, 256, 0, st>>>(q, s, qt, st_, static_cast<int>(M), static_cast<int>(K),
+                                         pow2 ? 1 : 0);
   return cudaGetLastError();
 }
 

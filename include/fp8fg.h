@@ -77,6 +77,25 @@ fp8fg_status fp8_act_quant(const void* x, fp8fg_dtype x_dtype, int64_t M, int64_
                            uint8_t* q, float* s, unsigned flags, void* stream);
 
 /*
+ * fp8_requant_transpose -- backward re-quantisation of stored FP8 activations.
+ * Source: page 5, backward-pass passage: the FP8 activations kept from the
+ * forward pass are dequantised, transposed and quantised again in 128x1 tiles
+ * (the operand layout the weight-gradient GEMM needs).
+ *
+ * q    [M, K] E4M3 codes with 1x128 scales s [M, K/128] (fp8_act_quant's
+ *      output layout), M % 128 == 0, K % 128 == 0.
+ * q_t  [K, M] codes, s_t [K, M/128] FP32: tile (k, i) = column k of the
+ *      dequantised matrix, rows 128i .. 128i+127, as fp8_act_quant with
+ *      FP8FG_TRANSPOSE would produce from it.
+ * Dequantisation: x = fl32(decode(q) * s[row, k/128]) (one IEEE multiply;
+ * E4M3 values are exact in FP32); then the scale rule of fp8_act_quant per
+ * 128x1 tile.  Flags: FP8FG_POW2 only.  q must hold no NaN codes.
+ * M may be 0 (nothing is launched).
+ */
+fp8fg_status fp8_requant_transpose(const uint8_t* q, const float* s, int64_t M, int64_t K,
+                                   uint8_t* q_t, float* s_t, unsigned flags, void* stream);
+
+/*
  * fp8_weight_quant -- online 128x128 block quantisation of weights to E4M3.
  * Source: page 1, Figure 7 (a) (one scale per 128 input x 128 output
  * channels) and "Storage Format" passage; page 2, online-amax passage.
@@ -141,7 +160,7 @@ fp8fg_status fp8_get_device_status(void* stream);
 /* Short English description of a status code (static storage). */
 const char* fp8fg_status_string(fp8fg_status status);
 
-/* ABI version of this header (bumped on any signature change). */
+/* ABI version of this header (bumped on any signature change or addition). */
 int fp8fg_abi_version(void);
 
 /*

@@ -40,7 +40,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_abi_version_and_status_strings(lib):
-    assert lib.fp8fg_abi_version() == 1
+    assert lib.fp8fg_abi_version() == 2
     for code in range(7):
         assert fp8.status_string(code)
     assert "unknown" in fp8.status_string(99)
@@ -73,6 +73,17 @@ def test_weight_quant_rejections(lib):
     assert f(A16, 0, 100, 128, A16, A16, None, None, 0, None) == fp8.ERR_UNSUPPORTED_SHAPE
     assert f(A16, 0, 128, 130, A16, A16, None, None, 0, None) == fp8.ERR_UNSUPPORTED_SHAPE
     assert f(A16, 0, 128, 128, MIS, A16, None, None, 0, None) == fp8.ERR_MISALIGNED
+
+
+def test_requant_transpose_rejections(lib):
+    f = lib.fp8_requant_transpose
+    assert f(A16, A16, 128, 128, A16, A16, fp8.TRANSPOSE, None) == fp8.ERR_INVALID_ARG  # flag
+    assert f(None, A16, 128, 128, A16, A16, 0, None) == fp8.ERR_INVALID_ARG
+    assert f(A16, A16, -128, 128, A16, A16, 0, None) == fp8.ERR_INVALID_ARG
+    assert f(A16, A16, 100, 128, A16, A16, 0, None) == fp8.ERR_UNSUPPORTED_SHAPE       # M % 128
+    assert f(A16, A16, 128, 200, A16, A16, 0, None) == fp8.ERR_UNSUPPORTED_SHAPE       # K % 128
+    assert f(A16, MIS, 128, 128, A16, A16, 0, None) == fp8.ERR_MISALIGNED
+    assert f(None, None, 0, 128, None, None, 0, None) == fp8.OK                     # M == 0
 
 
 def test_gemm_rejections(lib):

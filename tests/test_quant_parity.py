@@ -177,3 +177,67 @@ def test_moe_inputs_pow2_full_size(cuda_lib):
     h = synth.swiglu_like_bf16((case.rows, case.I), case.seed)
     q, s = cuda_lib.act_quant(h.cuda(), pow2=True)
     _assert_same(q, s, *H.oracle_act_quant_rows(H.f32(h), pow2=True))
+
+
+# ------------------------------------------------- backward re-quantisation (128x1 from FP8)
+def _stored_codes(M, K, seed, pow2=False):
+    z = synth.normal_f32((M, K), 1.0, seed, 77, outlier_p=0.01, outlier_mult=60.0)
+    return oracle.act_quant(z, pow2=pow2)
+
+
+@pytest.mark.parametrize("pow2", [False, True])
+@pytest.mark.parametrize("M,K", [(128, 128), (384, 640), (256, 1152)])
+def test_requant_transpose(cuda_lib, M, K, pow2):
+    q, s = _stored_codes(M, K, M + K)
+    raws = [H.guarded_empty(shp, dt) for shp, dt in (((K, M), torch.uint8),
+                                                     ((K, M // 128), torch.float32))]
+    qt, st = (b for _, b in raws)
+    q_d, s_d = H.to_dev(q), H.to_dev(s)          # keep the inputs alive across the launch
+    rc = cuda_lib.load().fp8_requant_transpose(q_d.data_ptr(), s_d.data_ptr(), M, K,
+                                               qt.data_ptr(), st.data_ptr(), 1 if pow2 else 0,
+                                               torch.cuda.current_stream().cuda_stream)
+    assert rc == 0
+    torch.cuda.synchronize()
+    assert all(H.guards_intact(r) for r, _ in raws)
+    _assert_same(qt, st, *oracle.requant_t(q, s, pow2=pow2))
+
+
+def test_requant_transpose_worked_block(cuda_lib):
+    # the hand-worked block of tests/golden/requant_t_worked.txt
+    q = np.empty((128, 256), np.uint8)
+    q[:, :128] = 0x38
+    q[:, 128::2] = 0x3C
+    q[:, 129::2] = 0xBC
+    s = np.empty((128, 2), np.float32)
+    s[:, 0] = 2.0 ** (np.arange(128) % 8)
+    s[:, 1] = 0.25
+    for pow2 in (False, True):
+        qt, st = cuda_lib.requant_transpose(H.to_dev(q), H.to_dev(s), pow2=pow2)
+        _assert_same(qt, st, *oracle.requant_t(q, s, pow2=pow2))
+
+
+def test_requant_transpose_edge_codes(cuda_lib):
+    # every finite code (signed zeros, subnormal codes, +-448) with widely
+    # different row scales, including scales that make the products subnormal
+    codes = np.arange(256, dtype=np.uint8)
+    codes = codes[(codes & 0x7F) != 0x7F]                       # drop the NaN codes
+    g = np.random.default_rng(8)
+    q = codes[g.integers(0, codes.size, (256, 256))].astype(np.uint8)
+    s = np.exp2(g.integers(-140, 60, (256, 2))).astype(np.float32)
+    s[5] = 0.0
+    qt, st = cuda_lib.requant_transpose(H.to_dev(q), H.to_dev(s))
+    _assert_same(qt, st, *oracle.requant_t(q, s))
+
+
+def test_requant_transpose_full_size(cuda_lib):
+    """The stored Fprop input X 4096x7168 (1x128) re-quantised for the Wgrad GEMM."""
+    x = synth.dense_case("fprop").x()
+    q, s = cuda_lib.act_quant(x.cuda())
+    qt, st = cuda_lib.requant_transpose(q, s)
+    q_r, s_r = H.oracle_act_quant_rows(H.f32(x))
+    assert np.array_equal(q.cpu().numpy(), q_r)
+    qt_r = np.empty((7168, 4096), np.uint8)
+    st_r = np.empty((7168, 32), np.float32)
+    for c in range(0, 7168, 1024):       # column groups of the oracle (tiles never cross columns)
+        qt_r[c:c + 1024], st_r[c:c + 1024] = oracle.requant_t(q_r[:, c:c + 1024], s_r[:, c // 128:(c + 1024) // 128])
+    _assert_same(qt, st, qt_r, st_r)
