@@ -36,8 +36,12 @@ fp8fg_status launch_grouped_gemm(const uint8_t* a, const float* sa, const int32_
 // Failure-detection self-test: one wait that nothing completes.
 cudaError_t launch_wait_timeout_selftest(uint32_t limit_cycles, cudaStream_t st);
 
-// Encode a 2D/3D uint8 tensor map (innermost dimension first) with 128-byte
-// swizzling and zero fill; returns false if the driver rejects it.
+// Encode a tensor map (innermost dimension first, zero fill); returns false if
+// the driver rejects it.
+bool encode_tensor_map(CUtensorMap* map, CUtensorMapDataType dtype, const void* base, int rank,
+                       const uint64_t* dims, const uint64_t* strides_bytes, const uint32_t* box,
+                       CUtensorMapSwizzle swizzle);
+// The same for uint8 elements with 128-byte swizzling (GEMM operand tiles).
 bool encode_tensor_map_u8(CUtensorMap* map, const void* base, int rank, const uint64_t* dims,
                           const uint64_t* strides_bytes, const uint32_t* box);
 

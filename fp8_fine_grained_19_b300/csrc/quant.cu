@@ -145,102 +145,156 @@ __global__ void __launch_bounds__(256) act_quant_rows_kernel(const T* __restrict
 }
 
 // --------------------------------------------------------------------------
-// 128x1 tiles along M, transposed output.  One CTA owns rows [128 i, 128 i+128)
-// and COLS columns of x (COLS = 128 for BF16, 64 for FP32: 32 KB either way),
-// staged raw in shared memory by coalesced 16-byte loads.  Thread (j, g) owns
-// the column pair (2j, 2j+1) and rows g*RPG.. of the block: it reads them as
-// 32- or 64-bit words (conflict-free), publishes its two partial amaxes, and
-// after one barrier reads them again, converts them and writes RPG code bytes
-// to each of q^T rows col0+2j and col0+2j+1.
+// 128x1 tiles along M, transposed output.  Persistent CTAs walk blocks of 128
+// rows x COLS columns of x (COLS = 128 for BF16, 64 for FP32: 32 KB either
+// way); TMA fills a 2-stage ring of such blocks in shared memory (3 CTAs of 512
+// threads per SM), so the threads only read columns, convert and store.
+// Thread (j, g) owns the column
+// pair (2j, 2j+1) and rows g*RPG.. of the block: it reads them as 32- or 64-bit
+// words (conflict-free: a block row is 256 contiguous bytes), publishes its two
+// partial amaxes, and after one barrier reads them again, converts them and
+// writes RPG code bytes to each of q^T rows col0+2j and col0+2j+1.
+constexpr int kColStages = 2;
+constexpr int kColThreads = 512;
+
 template <typename T>
-__global__ void __launch_bounds__(256) act_quant_cols_kernel(const T* __restrict__ x,
+struct ColTile {
+  static constexpr int ROWS = 128;
+  static constexpr int COLS = sizeof(T) == 2 ? 128 : 64;
+  static constexpr int BYTES = ROWS * COLS * static_cast<int>(sizeof(T));
+};
+
+template <typename T>
+__global__ void __launch_bounds__(kColThreads) act_quant_cols_kernel(const __grid_constant__ CUtensorMap tmX,
                                                              uint8_t* __restrict__ qt,
-                                                             float* __restrict__ st, int M,
-                                                             int K, int pow2) {
-  constexpr int ROWS = 128;
-  constexpr int COLS = sizeof(T) == 2 ? 128 : 64;
-  constexpr int EPV = Vec16<T>::N;            // elements per 16-byte vector
-  constexpr int VPR = COLS / EPV;             // vectors per tile row (16)
-  constexpr int NV = ROWS * VPR / 256;        // vectors per thread (8)
+                                                             float* __restrict__ st, int M, int K,
+                                                             int pow2, long long wait_limit,
+                                                             int* status) {
+  constexpr int ROWS = ColTile<T>::ROWS;
+  constexpr int COLS = ColTile<T>::COLS;
   constexpr int NPAIR = COLS / 2;             // column pairs
-  constexpr int RG = 256 / NPAIR;             // row groups (4 or 8)
-  constexpr int RPG = ROWS / RG;              // rows per group (32 or 16)
-  __shared__ __align__(16) T tile[ROWS][COLS];
+  constexpr int RG = kColThreads / NPAIR;     // row groups (8 or 16)
+  constexpr int RPG = ROWS / RG;              // rows per group (16 or 8)
+  extern __shared__ __align__(128) uint8_t qc_smem[];
+  T (*tiles)[ROWS][COLS] = reinterpret_cast<T (*)[ROWS][COLS]>(qc_smem);
+  __shared__ __align__(8) uint64_t full[kColStages];
   __shared__ float part[RG][COLS];
+  __shared__ __align__(16) uint8_t codes[RPG == 16 ? COLS : 1][128];   // BF16 path: staged q^T rows
+  __shared__ int abort_flag;
 
-  const int row0 = blockIdx.y * ROWS;
-  const int col0 = blockIdx.x * COLS;
   const int t = threadIdx.x;
-
-  uint4 v[NV];
-#pragma unroll
-  for (int i = 0; i < NV; ++i) {
-    const int vid = t + 256 * i;
-    const int r = vid / VPR, c = (vid % VPR) * EPV;
-    v[i] = ld_stream16(x + static_cast<int64_t>(row0 + r) * K + col0 + c);
-  }
-#pragma unroll
-  for (int i = 0; i < NV; ++i) {
-    const int vid = t + 256 * i;
-    const int r = vid / VPR, c = (vid % VPR) * EPV;
-    *reinterpret_cast<uint4*>(&tile[r][c]) = v[i];
+  const int col_tiles = K / COLS;
+  const int n_tiles = col_tiles * (M / ROWS);
+  if (t == 0) {
+    for (int s = 0; s < kColStages; ++s) mbar_init(smem_u32(&full[s]), 1);
+    fence_mbar_init();
+    abort_flag = 0;
+    tma_prefetch_desc(&tmX);
+    for (int s = 0; s < kColStages; ++s) {
+      const int tile = blockIdx.x + s * gridDim.x;
+      if (tile < n_tiles) {
+        mbar_arrive_expect_tx(smem_u32(&full[s]), ColTile<T>::BYTES);
+        tma_load_2d(smem_u32(&tiles[s][0][0]), &tmX, smem_u32(&full[s]), (tile % col_tiles) * COLS,
+                    (tile / col_tiles) * ROWS);
+      }
+    }
   }
   __syncthreads();
 
   const int j = t % NPAIR, g = t / NPAIR;
-  // the column pair (2j, 2j+1) at row r of this thread's group
-  auto pair_at = [&](int r, float& x0, float& x1) {
-    if constexpr (sizeof(T) == 2) {
-      const uint32_t w = *reinterpret_cast<const uint32_t*>(&tile[g * RPG + r][2 * j]);
-      x0 = __uint_as_float(w << 16);
-      x1 = __uint_as_float(w & 0xFFFF0000u);
-    } else {
-      const float2 w = *reinterpret_cast<const float2*>(&tile[g * RPG + r][2 * j]);
-      x0 = w.x;
-      x1 = w.y;
+  int i = 0;
+  for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x, ++i) {
+    const int stg = i % kColStages;
+    const bool got =
+        mbar_wait(smem_u32(&full[stg]), (i / kColStages) & 1, wait_limit, &abort_flag, status);
+    if (__syncthreads_or(!got)) break;
+    const int col0 = (tile % col_tiles) * COLS;
+    const int rb = tile / col_tiles;
+    const int row0 = rb * ROWS;
+    T (*blk)[COLS] = tiles[stg];
+    // the column pair (2j, 2j+1) at row r of this thread's group
+    auto pair_at = [&](int r, float& x0, float& x1) {
+      if constexpr (sizeof(T) == 2) {
+        const uint32_t w = *reinterpret_cast<const uint32_t*>(&blk[g * RPG + r][2 * j]);
+        x0 = __uint_as_float(w << 16);
+        x1 = __uint_as_float(w & 0xFFFF0000u);
+      } else {
+        const float2 w = *reinterpret_cast<const float2*>(&blk[g * RPG + r][2 * j]);
+        x0 = w.x;
+        x1 = w.y;
+      }
+    };
+    float a0 = 0.0f, a1 = 0.0f;
+#pragma unroll
+    for (int r = 0; r < RPG; ++r) {
+      float x0, x1;
+      pair_at(r, x0, x1);
+      a0 = fmaxf(a0, fabsf(x0));
+      a1 = fmaxf(a1, fabsf(x1));
     }
-  };
-  float a0 = 0.0f, a1 = 0.0f;
+    part[g][2 * j] = a0;
+    part[g][2 * j + 1] = a1;
+    __syncthreads();
 #pragma unroll
-  for (int r = 0; r < RPG; ++r) {
-    float x0, x1;
-    pair_at(r, x0, x1);
-    a0 = fmaxf(a0, fabsf(x0));
-    a1 = fmaxf(a1, fabsf(x1));
+    for (int k = 0; k < RG; ++k) {
+      a0 = fmaxf(a0, part[k][2 * j]);
+      a1 = fmaxf(a1, part[k][2 * j + 1]);
+    }
+    const Scale s0 = scale_from_amax(a0, pow2 != 0);
+    const Scale s1 = scale_from_amax(a1, pow2 != 0);
+    if (g == 0) {
+      st[static_cast<int64_t>(col0 + 2 * j) * (M / ROWS) + rb] = s0.s;
+      st[static_cast<int64_t>(col0 + 2 * j + 1) * (M / ROWS) + rb] = s1.s;
+    }
+    uint32_t w0[RPG / 4], w1[RPG / 4];
+#pragma unroll
+    for (int q4 = 0; q4 < RPG / 4; ++q4) {
+      float x[4], y[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) pair_at(4 * q4 + e, x[e], y[e]);
+      w0[q4] = e4m3x2(__fmul_rn(x[0], s0.m), __fmul_rn(x[1], s0.m)) |
+               (e4m3x2(__fmul_rn(x[2], s0.m), __fmul_rn(x[3], s0.m)) << 16);
+      w1[q4] = e4m3x2(__fmul_rn(y[0], s1.m), __fmul_rn(y[1], s1.m)) |
+               (e4m3x2(__fmul_rn(y[2], s1.m), __fmul_rn(y[3], s1.m)) << 16);
+    }
+    if constexpr (RPG == 16) {
+      // Stage the codes as q^T rows (128 bytes each) in shared memory, 16-byte
+      // chunk c of row k at position c ^ ((k / 2) % 8): the chunk writes below
+      // and the row reads of the copy-out both use every bank once per
+      // 128-byte wavefront.  The copy-out then writes whole 128-byte lines.
+      *reinterpret_cast<uint4*>(&codes[2 * j][16 * (g ^ (j % 8))]) =
+          make_uint4(w0[0], w0[1], w0[2], w0[3]);
+      *reinterpret_cast<uint4*>(&codes[2 * j + 1][16 * (g ^ (j % 8))]) =
+          make_uint4(w1[0], w1[1], w1[2], w1[3]);
+      __syncthreads();
+#pragma unroll
+      for (int q16 = 0; q16 < COLS * 8 / kColThreads; ++q16) {
+        const int ci = t + kColThreads * q16;
+        const int k = ci / 8, c = ci % 8;
+        const uint4 v = *reinterpret_cast<const uint4*>(&codes[k][16 * (c ^ ((k / 2) % 8))]);
+        *reinterpret_cast<uint4*>(qt + static_cast<int64_t>(col0 + k) * M + row0 + 16 * c) = v;
+      }
+    } else {
+      uint8_t* d0 = qt + static_cast<int64_t>(col0 + 2 * j) * M + row0 + g * RPG;
+      uint8_t* d1 = qt + static_cast<int64_t>(col0 + 2 * j + 1) * M + row0 + g * RPG;
+      *reinterpret_cast<uint2*>(d0) = make_uint2(w0[0], w0[1]);
+      *reinterpret_cast<uint2*>(d1) = make_uint2(w1[0], w1[1]);
+    }
+    // every thread is done with this stage, part[] and codes[]: refill it
+    __syncthreads();
+    if (t == 0) {
+      const int next = tile + kColStages * gridDim.x;
+      if (next < n_tiles) {
+        mbar_arrive_expect_tx(smem_u32(&full[stg]), ColTile<T>::BYTES);
+        tma_load_2d(smem_u32(&tiles[stg][0][0]), &tmX, smem_u32(&full[stg]),
+                    (next % col_tiles) * COLS, (next / col_tiles) * ROWS);
+      }
+    }
   }
-  part[g][2 * j] = a0;
-  part[g][2 * j + 1] = a1;
-  __syncthreads();
-#pragma unroll
-  for (int i = 0; i < RG; ++i) {
-    a0 = fmaxf(a0, part[i][2 * j]);
-    a1 = fmaxf(a1, part[i][2 * j + 1]);
-  }
-  const Scale s0 = scale_from_amax(a0, pow2 != 0);
-  const Scale s1 = scale_from_amax(a1, pow2 != 0);
-  if (g == 0) {
-    st[static_cast<int64_t>(col0 + 2 * j) * (M / ROWS) + blockIdx.y] = s0.s;
-    st[static_cast<int64_t>(col0 + 2 * j + 1) * (M / ROWS) + blockIdx.y] = s1.s;
-  }
-  // second pass over the same shared words (cheaper than holding 2 x RPG
-  // values in registers, which would cap the CTAs per SM)
-  uint32_t w0[RPG / 4], w1[RPG / 4];
-#pragma unroll
-  for (int i = 0; i < RPG / 4; ++i) {
-    float x[4], y[4];
-#pragma unroll
-    for (int e = 0; e < 4; ++e) pair_at(4 * i + e, x[e], y[e]);
-    w0[i] = e4m3x2(__fmul_rn(x[0], s0.m), __fmul_rn(x[1], s0.m)) |
-            (e4m3x2(__fmul_rn(x[2], s0.m), __fmul_rn(x[3], s0.m)) << 16);
-    w1[i] = e4m3x2(__fmul_rn(y[0], s1.m), __fmul_rn(y[1], s1.m)) |
-            (e4m3x2(__fmul_rn(y[2], s1.m), __fmul_rn(y[3], s1.m)) << 16);
-  }
-  uint4* d0 = reinterpret_cast<uint4*>(qt + static_cast<int64_t>(col0 + 2 * j) * M + row0 + g * RPG);
-  uint4* d1 = reinterpret_cast<uint4*>(qt + static_cast<int64_t>(col0 + 2 * j + 1) * M + row0 + g * RPG);
-#pragma unroll
-  for (int i = 0; i < RPG / 16; ++i) {
-    d0[i] = make_uint4(w0[4 * i], w0[4 * i + 1], w0[4 * i + 2], w0[4 * i + 3]);
-    d1[i] = make_uint4(w1[4 * i], w1[4 * i + 1], w1[4 * i + 2], w1[4 * i + 3]);
+  // after an abort, let copies still in flight land before the CTA exits
+  if (abort_flag && t == 0) {
+    const long long t0 = clock64();
+    while (clock64() - t0 < (1 << 20)) __nanosleep(1000);
   }
 }
 
@@ -251,8 +305,8 @@ __global__ void __launch_bounds__(256) act_quant_cols_kernel(const T* __restrict
 // of one scale group, so each row has a single scale: the 16 KB code block and
 // the 128 row scales are staged in shared memory.  Thread (j, g) owns the
 // column pair (2j, 2j+1) and rows 32g..32g+31; as in act_quant_cols it takes
-// the column amax in a first pass and converts in a second, writing 32 code
-// bytes to each of q^T rows col0+2j and col0+2j+1.
+// the column amax in a first pass and converts in a second; the codes are then
+// staged as q^T rows in shared memory and written as whole 128-byte rows.
 __device__ __forceinline__ void e4m3x2_to_f32(uint32_t two_codes, float& lo, float& hi) {
   uint32_t h2;   // E4M3 -> FP16 is exact (E4M3 is a subset of FP16)
   asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(static_cast<uint16_t>(two_codes)));
@@ -332,12 +386,26 @@ __global__ void __launch_bounds__(256) requant_t_kernel(const uint8_t* __restric
     w1[i] = e4m3x2(__fmul_rn(y[0], s1.m), __fmul_rn(y[1], s1.m)) |
             (e4m3x2(__fmul_rn(y[2], s1.m), __fmul_rn(y[3], s1.m)) << 16);
   }
-  uint4* d0 = reinterpret_cast<uint4*>(qt + static_cast<int64_t>(col0 + 2 * j) * M + row0 + g * RPG);
-  uint4* d1 = reinterpret_cast<uint4*>(qt + static_cast<int64_t>(col0 + 2 * j + 1) * M + row0 + g * RPG);
-  d0[0] = make_uint4(w0[0], w0[1], w0[2], w0[3]);
-  d0[1] = make_uint4(w0[4], w0[5], w0[6], w0[7]);
-  d1[0] = make_uint4(w1[0], w1[1], w1[2], w1[3]);
-  d1[1] = make_uint4(w1[4], w1[5], w1[6], w1[7]);
+  // stage the codes as q^T rows in the (no longer needed) code tile, 16-byte
+  // chunk c of row k at position c ^ ((k / 2) % 8), then write whole rows
+  __syncthreads();
+  uint8_t (*out)[COLS] = tile;
+  const int sw = j % 8;
+  *reinterpret_cast<uint4*>(&out[2 * j][16 * ((2 * g) ^ sw)]) = make_uint4(w0[0], w0[1], w0[2], w0[3]);
+  *reinterpret_cast<uint4*>(&out[2 * j][16 * ((2 * g + 1) ^ sw)]) =
+      make_uint4(w0[4], w0[5], w0[6], w0[7]);
+  *reinterpret_cast<uint4*>(&out[2 * j + 1][16 * ((2 * g) ^ sw)]) =
+      make_uint4(w1[0], w1[1], w1[2], w1[3]);
+  *reinterpret_cast<uint4*>(&out[2 * j + 1][16 * ((2 * g + 1) ^ sw)]) =
+      make_uint4(w1[4], w1[5], w1[6], w1[7]);
+  __syncthreads();
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int ci = t + 256 * i;
+    const int k = ci / 8, c = ci % 8;
+    const uint4 v = *reinterpret_cast<const uint4*>(&out[k][16 * (c ^ ((k / 2) % 8))]);
+    *reinterpret_cast<uint4*>(qt + static_cast<int64_t>(col0 + k) * M + row0 + 16 * c) = v;
+  }
 }
 
 // --------------------------------------------------------------------------
@@ -444,13 +512,28 @@ __global__ void __launch_bounds__(256) weight_quant_kernel(const T* __restrict__
       w1[i] = e4m3x2(__fmul_rn(y[0], sc.m), __fmul_rn(y[1], sc.m)) |
               (e4m3x2(__fmul_rn(y[2], sc.m), __fmul_rn(y[3], sc.m)) << 16);
     }
-    uint4* d0 = reinterpret_cast<uint4*>(qt + static_cast<int64_t>(col0 + 2 * j) * N + row0 + 32 * g);
-    uint4* d1 =
-        reinterpret_cast<uint4*>(qt + static_cast<int64_t>(col0 + 2 * j + 1) * N + row0 + 32 * g);
-    d0[0] = make_uint4(w0[0], w0[1], w0[2], w0[3]);
-    d0[1] = make_uint4(w0[4], w0[5], w0[6], w0[7]);
-    d1[0] = make_uint4(w1[0], w1[1], w1[2], w1[3]);
-    d1[1] = make_uint4(w1[4], w1[5], w1[6], w1[7]);
+    // stage the codes as q^T rows in the block's shared memory (no longer
+    // read), 16-byte chunk c of row k at position c ^ ((k / 2) % 8), then
+    // write whole 128-byte rows of q^T
+    __syncthreads();
+    uint8_t (*out)[B] = reinterpret_cast<uint8_t (*)[B]>(wq_smem);
+    const int sw = j % 8;
+    *reinterpret_cast<uint4*>(&out[2 * j][16 * ((2 * g) ^ sw)]) =
+        make_uint4(w0[0], w0[1], w0[2], w0[3]);
+    *reinterpret_cast<uint4*>(&out[2 * j][16 * ((2 * g + 1) ^ sw)]) =
+        make_uint4(w0[4], w0[5], w0[6], w0[7]);
+    *reinterpret_cast<uint4*>(&out[2 * j + 1][16 * ((2 * g) ^ sw)]) =
+        make_uint4(w1[0], w1[1], w1[2], w1[3]);
+    *reinterpret_cast<uint4*>(&out[2 * j + 1][16 * ((2 * g + 1) ^ sw)]) =
+        make_uint4(w1[4], w1[5], w1[6], w1[7]);
+    __syncthreads();
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int ci = t + 256 * i;
+      const int k = ci / 8, c = ci % 8;
+      const uint4 v = *reinterpret_cast<const uint4*>(&out[k][16 * (c ^ ((k / 2) % 8))]);
+      *reinterpret_cast<uint4*>(qt + static_cast<int64_t>(col0 + k) * N + row0 + 16 * c) = v;
+    }
   }
 }
 
@@ -477,16 +560,34 @@ cudaError_t launch_act_quant_rows(const void* x, fp8fg_dtype xt, int64_t M, int6
 
 cudaError_t launch_act_quant_cols(const void* x, fp8fg_dtype xt, int64_t M, int64_t K, uint8_t* qt,
                                   float* st_, bool pow2, cudaStream_t st) {
-  const unsigned cols = xt == FP8FG_BF16 ? 128 : 64;    // columns per CTA (K % 128 == 0)
-  const dim3 grid(static_cast<unsigned>(K / cols), static_cast<unsigned>(M / 128));
-  if (xt == FP8FG_BF16)
-    act_quant_cols_kernel<__nv_bfloat16><<<grid, 256, 0, st>>>(
-        static_cast<const __nv_bfloat16*>(x), qt, st_, static_cast<int>(M), static_cast<int>(K),
-        pow2 ? 1 : 0);
-  else
-    act_quant_cols_kernel<float><<<grid, 256, 0, st>>>(static_cast<const float*>(x), qt, st_,
-                                                       static_cast<int>(M), static_cast<int>(K),
-                                                       pow2 ? 1 : 0);
+  const bool bf16 = xt == FP8FG_BF16;
+  const int cols = bf16 ? ColTile<__nv_bfloat16>::COLS : ColTile<float>::COLS;
+  const uint64_t dims[2] = {static_cast<uint64_t>(K), static_cast<uint64_t>(M)};
+  const uint64_t strides[1] = {static_cast<uint64_t>(K) * (bf16 ? 2 : 4)};
+  const uint32_t box[2] = {static_cast<uint32_t>(cols), 128};
+  CUtensorMap map;
+  if (!encode_tensor_map(&map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
+                         x, 2, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_NONE))
+    return cudaErrorInvalidValue;
+  const int64_t n_tiles = (K / cols) * (M / 128);
+  const int64_t max_ctas = static_cast<int64_t>(device_sm_count()) * 3;   // 3 x 64 KB per SM
+  const int grid = static_cast<int>(n_tiles < max_ctas ? n_tiles : max_ctas);
+  const int smem = kColStages * 32768;
+  if (bf16) {
+    static const cudaError_t attr = cudaFuncSetAttribute(
+        act_quant_cols_kernel<__nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (attr != cudaSuccess) return attr;
+    act_quant_cols_kernel<__nv_bfloat16><<<grid, kColThreads, smem, st>>>(
+        map, qt, st_, static_cast<int>(M), static_cast<int>(K), pow2 ? 1 : 0, wait_limit_cycles(),
+        device_status_word());
+  } else {
+    static const cudaError_t attr = cudaFuncSetAttribute(
+        act_quant_cols_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (attr != cudaSuccess) return attr;
+    act_quant_cols_kernel<float><<<grid, kColThreads, smem, st>>>(
+        map, qt, st_, static_cast<int>(M), static_cast<int>(K), pow2 ? 1 : 0, wait_limit_cycles(),
+        device_status_word());
+  }
   return cudaGetLastError();
 }
 
