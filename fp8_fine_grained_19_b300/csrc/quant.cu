@@ -111,19 +111,37 @@ __global__ void __launch_bounds__(256) act_quant_rows_kernel(const T* __restrict
       const int64_t tile = base + u * TPW + tsel;
       v[u] = tile < n_tiles ? ld_stream16(x + tile * 128 + sub * EPL) : make_uint4(0, 0, 0, 0);
     }
+    // tile amaxes (every lane of a tile ends with its tile's amax)
+    float amax[UNROLL];
+#pragma unroll
+    for (int u = 0; u < UNROLL; ++u) {
+      float f[EPL];
+      Vec16<T>::unpack(v[u], f);
+      float a = 0.0f;
+#pragma unroll
+      for (int i = 0; i < EPL; ++i) a = fmaxf(a, fabsf(f[i]));
+#pragma unroll
+      for (int off = LPT / 2; off > 0; off >>= 1)
+        a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, off));
+      amax[u] = a;
+    }
+    // lane L < CHUNK derives the scale of tile (u = L / TPW, tile-in-vector
+    // L % TPW) once, instead of every lane of every tile doing it
+    float my_amax = 0.0f;
+#pragma unroll
+    for (int u = 0; u < UNROLL; ++u) {
+      const float a = __shfl_sync(0xFFFFFFFFu, amax[u], (lane % TPW) * LPT);
+      if (lane / TPW == u) my_amax = a;
+    }
+    const Scale mine = scale_from_amax(my_amax, pow2 != 0);
 #pragma unroll
     for (int u = 0; u < UNROLL; ++u) {
       const int64_t tile = base + u * TPW + tsel;
       float f[EPL];
       Vec16<T>::unpack(v[u], f);
-      float amax = 0.0f;
-#pragma unroll
-      for (int i = 0; i < EPL; ++i) amax = fmaxf(amax, fabsf(f[i]));
-#pragma unroll
-      for (int off = LPT / 2; off > 0; off >>= 1)
-        amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, off));
+      const int src = u * TPW + tsel;
+      const Scale sc = {__shfl_sync(0xFFFFFFFFu, mine.s, src), __shfl_sync(0xFFFFFFFFu, mine.m, src)};
       if (tile < n_tiles) {
-        const Scale sc = scale_from_amax(amax, pow2 != 0);
         uint32_t packed[EPL / 4];
 #pragma unroll
         for (int i = 0; i < EPL / 4; ++i) {
@@ -179,6 +197,7 @@ __global__ void __launch_bounds__(kColThreads) act_quant_cols_kernel(const __gri
   T (*tiles)[ROWS][COLS] = reinterpret_cast<T (*)[ROWS][COLS]>(qc_smem);
   __shared__ __align__(8) uint64_t full[kColStages];
   __shared__ float part[RG][COLS];
+  __shared__ float colm[COLS];                                          // per-column multipliers
   __shared__ __align__(16) uint8_t codes[RPG == 16 ? COLS : 1][128];   // BF16 path: staged q^T rows
   __shared__ int abort_flag;
 
@@ -235,17 +254,18 @@ __global__ void __launch_bounds__(kColThreads) act_quant_cols_kernel(const __gri
     part[g][2 * j] = a0;
     part[g][2 * j + 1] = a1;
     __syncthreads();
+    // one thread per column folds the partials and derives the scale once
+    if (t < COLS) {
+      float a = part[0][t];
 #pragma unroll
-    for (int k = 0; k < RG; ++k) {
-      a0 = fmaxf(a0, part[k][2 * j]);
-      a1 = fmaxf(a1, part[k][2 * j + 1]);
+      for (int k = 1; k < RG; ++k) a = fmaxf(a, part[k][t]);
+      const Scale sc = scale_from_amax(a, pow2 != 0);
+      colm[t] = sc.m;
+      st[static_cast<int64_t>(col0 + t) * (M / ROWS) + rb] = sc.s;
     }
-    const Scale s0 = scale_from_amax(a0, pow2 != 0);
-    const Scale s1 = scale_from_amax(a1, pow2 != 0);
-    if (g == 0) {
-      st[static_cast<int64_t>(col0 + 2 * j) * (M / ROWS) + rb] = s0.s;
-      st[static_cast<int64_t>(col0 + 2 * j + 1) * (M / ROWS) + rb] = s1.s;
-    }
+    __syncthreads();
+    const Scale s0 = {0.0f, colm[2 * j]};
+    const Scale s1 = {0.0f, colm[2 * j + 1]};
     uint32_t w0[RPG / 4], w1[RPG / 4];
 #pragma unroll
     for (int q4 = 0; q4 < RPG / 4; ++q4) {
