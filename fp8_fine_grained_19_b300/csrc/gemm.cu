@@ -25,6 +25,14 @@
 //               slice's partial, so the MMA of slice kb+1 overlaps the
 //               promotion of slice kb, and the next tile's MMAs overlap this
 //               tile's final store.
+// Output (dense): each promotion warp converts its 32 x 128 block chunk by
+// chunk (32 rows x 64 bytes) into a 2 KB shared staging buffer laid out in the
+// tensor map's 64-byte swizzle and writes it with one TMA tile store, which
+// clips at the matrix bounds.  Per-thread row stores (16 bytes into 32
+// different rows per instruction) take two to three times as long, and the
+// tensor pipe idles meanwhile.  The grouped kernel keeps per-thread row stores,
+// masked at each expert's end: with the staging code its K loop no longer
+// fits the promotion warps' registers and spills (measured 35% slower).
 // Tiles are visited in groups of 16 M-tiles (all N-tiles of a group before the
 // next), so a group's A rows stay in L2 while B streams once per group.
 // Every pipeline wait is bounded (FP8FG_ERR_TIMEOUT, see device_common.cuh).
@@ -59,6 +67,8 @@ constexpr int TMEM_COLS = 512;
 constexpr int GROUP_M = 16;
 constexpr int MAX_EXPERTS = 1024;
 constexpr int SB_GROUP = 8;           // tile mode: slices whose B scales are shared per barrier
+constexpr int CST_BYTES = 2048;       // output staging per promotion warp: 32 rows x 64 bytes
+constexpr int CST_ROW = 64;           // bytes per staged row (the tensor map's 64-byte swizzle)
 constexpr uint32_t IDESC = idesc_e4m3_f32(BM, BN);
 
 struct GemmParams {
@@ -79,6 +89,15 @@ struct GemmParams {
 struct Smem {
   uint8_t a[STAGES][A_BYTES];     // 1024-byte aligned (offset 0)
   uint8_t b[STAGES][B_BYTES];
+  // Tile-mode B scales ([column half][group parity][slice][col], read as
+  // float4) during a tile's K loop; output staging of the promotion warps
+  // after it.  Warp w stages in bytes [2 KB w, 2 KB (w+1)), inside the scale
+  // ring of its own column half, and the half synchronises before the ring
+  // is rewritten.
+  union alignas(1024) {
+    float sbt[2][2][SB_GROUP][128];
+    uint8_t cst[NUM_EPI_WARPS][CST_BYTES];
+  };
   uint64_t full_bar[STAGES];
   uint64_t empty_bar[STAGES];
   uint64_t tfull_bar[2];
@@ -88,13 +107,14 @@ struct Smem {
   int abort_flag;
   int bad_offsets;
   int num_tiles;
-  // tile-mode B scales: [column half][group parity][slice][col]; read as float4
-  alignas(16) float sbt[2][2][SB_GROUP][128];
   int cum[MAX_EXPERTS + 1];       // grouped: tile prefix per expert
   int row0[MAX_EXPERTS + 1];      // grouped: copy of offsets
 };
 
-static_assert(offsetof(Smem, sbt) % 16 == 0, "float4 reads of the tile-mode scales");
+static_assert(sizeof(Smem::sbt) == sizeof(Smem::cst), "staging spans the scale ring");
+static_assert(sizeof(Smem::sbt) / 2 == 4 * CST_BYTES, "a half's staging lies in its own ring");
+static_assert(offsetof(Smem, cst) % 1024 == 0, "swizzled TMA staging is 1024-byte aligned");
+static_assert(CST_BYTES == 32 * CST_ROW, "one staged chunk: 32 rows");
 static_assert(offsetof(Smem, full_bar) % 8 == 0, "mbarriers are 8-byte aligned");
 
 struct Tile {
@@ -143,7 +163,8 @@ __device__ __forceinline__ Tile tile_of(int t, const GemmParams& p, const Smem& 
 template <bool GROUPED, bool BTILE>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     blockscaled_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
-                            const __grid_constant__ CUtensorMap tmB, const GemmParams p) {
+                            const __grid_constant__ CUtensorMap tmB,
+                            const __grid_constant__ CUtensorMap tmC, const GemmParams p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   // 1024-byte alignment of the operand stages (required by the 128B swizzle)
   Smem& sm = *reinterpret_cast<Smem*>(
@@ -171,6 +192,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   if (warp == PRODUCER_WARP && lane == 0) {
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
+    tma_prefetch_desc(&tmC);
   }
   if constexpr (GROUPED) {
     // Copy and check the offsets, then prefix the per-expert tile counts with
@@ -306,6 +328,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const int n_blocks = p.N / 128;                 // block-mode scale rows per expert
     const uint32_t lane_taddr = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + half * 128;
     uint32_t it = 0;
+    bool staged = false;                            // a store of this warp may still read cst
     bool ok = true;
     for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
       const Tile tl = tile_of<GROUPED>(t, p, sm);
@@ -421,25 +444,24 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         if (!ok) break;
       }
 
-      // --- store this thread's row segment (128 columns of its half)
-      if (row_ok && half_ok) {
-        if (p.c_f32) {
-          float* dst = static_cast<float*>(p.c) + static_cast<int64_t>(row) * p.N + col_h;
+      if constexpr (GROUPED) {
+        // --- grouped: each thread stores its row segment (128 columns of its
+        // half); rows past the expert's end belong to the next expert
+        if (row_ok && half_ok) {
+          if (p.c_f32) {
+            float* dst = static_cast<float*>(p.c) + static_cast<int64_t>(row) * p.N + col_h;
 #pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            if (col_h + 4 * j + 4 <= p.N) {
+            for (int j = 0; j < 32; ++j) {
               float x0, x1, x2, x3;
               unpack2(acc[2 * j], x0, x1);
               unpack2(acc[2 * j + 1], x2, x3);
               *reinterpret_cast<float4*>(dst + 4 * j) = make_float4(x0, x1, x2, x3);
             }
-          }
-        } else {
-          __nv_bfloat16* dst =
-              static_cast<__nv_bfloat16*>(p.c) + static_cast<int64_t>(row) * p.N + col_h;
+          } else {
+            __nv_bfloat16* dst =
+                static_cast<__nv_bfloat16*>(p.c) + static_cast<int64_t>(row) * p.N + col_h;
 #pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            if (col_h + 8 * j + 8 <= p.N) {
+            for (int j = 0; j < 16; ++j) {
               uint32_t w[4];
 #pragma unroll
               for (int i = 0; i < 4; ++i) {
@@ -452,8 +474,71 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             }
           }
         }
+      } else {
+        // --- dense: the warp's 32 rows x 128 columns of its half go out in
+        // chunks of 64 bytes per row.  Chunk q of row `lane` goes to staging
+        // row `lane`, its 16-byte unit u at unit u ^ ((lane/2) % 4) (the 64-byte
+        // swizzle), so a warp's st.shared.v4 hits every bank once per 8 lanes;
+        // one TMA store writes the chunk and clips rows at or past M.
+        const int wrow0 = tl.m0 + quad * 32;
+        if (half_ok && wrow0 < p.M) {
+          // formed here rather than hoisted out of the tile loop, so that they
+          // hold no registers during the K loop
+          uint32_t wl = (warp << 8) | lane;
+          asm volatile("" : "+r"(wl));
+          const uint32_t cbuf = smem_u32(sm.cst[0]) + (wl >> 8) * CST_BYTES;
+          const uint32_t srow = cbuf + (wl & 31) * CST_ROW;
+          const uint32_t swz = ((wl & 31) >> 1) & 3;
+          const int W = p.c_f32 ? 16 : 32;        // columns per chunk
+#pragma unroll
+          for (int q = 0; q < 8; ++q) {
+            if ((p.c_f32 || q < 4) && col_h + q * W < p.N) {
+              if (staged) {
+                if (lane == 0) bulk_wait_read_all();
+                __syncwarp();
+              }
+#pragma unroll
+              for (int u = 0; u < 4; ++u) {
+                uint32_t w[4];
+                if (p.c_f32) {
+                  // columns 16q + 4u .. +3 = accumulator pairs 8q + 2u, +1
+                  const uint64_t x0 = acc[8 * q + 2 * u], x1 = acc[8 * q + 2 * u + 1];
+                  w[0] = static_cast<uint32_t>(x0);
+                  w[1] = static_cast<uint32_t>(x0 >> 32);
+                  w[2] = static_cast<uint32_t>(x1);
+                  w[3] = static_cast<uint32_t>(x1 >> 32);
+                } else {
+                  // columns 32q + 8u .. +7 = accumulator pairs 16q + 4u .. +3
+#pragma unroll
+                  for (int i = 0; i < 4; ++i) {
+                    float lo, hi;
+                    unpack2(acc[(16 * q + 4 * u + i) & 63], lo, hi);
+                    const __nv_bfloat162 b2 = __floats2bfloat162_rn(lo, hi);
+                    w[i] = *reinterpret_cast<const uint32_t*>(&b2);
+                  }
+                }
+                sts_128(srow + ((u ^ swz) << 4), w[0], w[1], w[2], w[3]);
+              }
+              fence_proxy_async_smem();
+              __syncwarp();
+              if (lane == 0) {
+                tma_store_2d(&tmC, cbuf, col_h + q * W, wrow0);
+                bulk_commit();
+              }
+              staged = true;
+            }
+          }
+        }
+      }
+      if constexpr (BTILE) {
+        // the next tile's scale ring overwrites this half's staging
+        if (lane == 0) bulk_wait_read_all();
+        __syncwarp();
+        bar_sync(1 + half, 128);
       }
     }
+    // the CTA's shared memory must outlive the reads of the last stores
+    if (lane == 0) bulk_wait_all();
   }
 
   // -------------------------------------------------------------- teardown
@@ -500,6 +585,18 @@ bool make_maps(CUtensorMap* mA, CUtensorMap* mB, const uint8_t* a, int64_t rowsA
   return encode_tensor_map_u8(mB, b, 3, dB, sB, boxB);
 }
 
+// C [rows, N] row-major, stored by 32-row x 64-byte boxes (16 FP32 or 32 BF16
+// columns) from 64-byte-swizzled staging.
+bool make_c_map(CUtensorMap* mC, void* c, fp8fg_dtype ct, int64_t rows, int64_t N) {
+  const bool f32 = ct == FP8FG_F32;
+  const uint64_t elt = f32 ? 4 : 2;
+  const uint64_t dC[2] = {static_cast<uint64_t>(N), static_cast<uint64_t>(rows)};
+  const uint64_t sC[1] = {static_cast<uint64_t>(N) * elt};
+  const uint32_t boxC[2] = {static_cast<uint32_t>(CST_ROW / elt), 32};
+  return encode_tensor_map(mC, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                           c, 2, dC, sC, boxC, CU_TENSOR_MAP_SWIZZLE_64B);
+}
+
 template <bool GROUPED, bool BTILE>
 cudaError_t set_smem_attr() {
   static const cudaError_t e = cudaFuncSetAttribute(
@@ -513,8 +610,9 @@ cudaError_t set_smem_attr() {
 fp8fg_status launch_gemm(const uint8_t* a, const float* sa, const uint8_t* b, const float* sb,
                          void* c, fp8fg_dtype ct, int64_t M, int64_t N, int64_t K, bool b_tile,
                          cudaStream_t st) {
-  CUtensorMap mA, mB;
-  if (!make_maps(&mA, &mB, a, M, b, 0, N, K)) return FP8FG_ERR_CUDA;
+  CUtensorMap mA, mB, mC;
+  if (!make_maps(&mA, &mB, a, M, b, 0, N, K) || !make_c_map(&mC, c, ct, M, N))
+    return FP8FG_ERR_CUDA;
   if ((b_tile ? set_smem_attr<false, true>() : set_smem_attr<false, false>()) != cudaSuccess)
     return FP8FG_ERR_CUDA;
   GemmParams p{};
@@ -536,18 +634,20 @@ fp8fg_status launch_gemm(const uint8_t* a, const float* sa, const uint8_t* b, co
   const int tiles = p.m_tiles * p.n_tiles;
   const int grid = tiles < device_sm_count() ? tiles : device_sm_count();
   if (b_tile)
-    blockscaled_gemm_kernel<false, true><<<grid, NUM_THREADS, kSmemBytes, st>>>(mA, mB, p);
+    blockscaled_gemm_kernel<false, true><<<grid, NUM_THREADS, kSmemBytes, st>>>(mA, mB, mC, p);
   else
-    blockscaled_gemm_kernel<false, false><<<grid, NUM_THREADS, kSmemBytes, st>>>(mA, mB, p);
+    blockscaled_gemm_kernel<false, false><<<grid, NUM_THREADS, kSmemBytes, st>>>(mA, mB, mC, p);
   return cudaGetLastError() == cudaSuccess ? FP8FG_OK : FP8FG_ERR_CUDA;
 }
 
 fp8fg_status launch_grouped_gemm(const uint8_t* a, const float* sa, const int32_t* offsets,
                                  int32_t E, int64_t total_rows, const uint8_t* b, const float* sb,
                                  void* c, fp8fg_dtype ct, int64_t N, int64_t K, cudaStream_t st) {
-  CUtensorMap mA, mB;
-  // an empty A (no rows) still needs a valid map: point it at one row
-  if (!make_maps(&mA, &mB, a, total_rows > 0 ? total_rows : 1, b, E, N, K)) return FP8FG_ERR_CUDA;
+  CUtensorMap mA, mB, mC;
+  // an empty A (no rows) still needs valid maps: point them at one row
+  const int64_t map_rows = total_rows > 0 ? total_rows : 1;
+  if (!make_maps(&mA, &mB, a, map_rows, b, E, N, K) || !make_c_map(&mC, c, ct, map_rows, N))
+    return FP8FG_ERR_CUDA;
   if (set_smem_attr<true, false>() != cudaSuccess) return FP8FG_ERR_CUDA;
   GemmParams p{};
   p.sa = sa;
@@ -565,7 +665,8 @@ fp8fg_status launch_grouped_gemm(const uint8_t* a, const float* sa, const int32_
   p.b_tile = 0;
   p.wait_limit = wait_limit_cycles();
   p.status = device_status_word();
-  blockscaled_gemm_kernel<true, false><<<device_sm_count(), NUM_THREADS, kSmemBytes, st>>>(mA, mB, p);
+  blockscaled_gemm_kernel<true, false><<<device_sm_count(), NUM_THREADS, kSmemBytes, st>>>(mA, mB,
+                                                                                          mC, p);
   return cudaGetLastError() == cudaSuccess ? FP8FG_OK : FP8FG_ERR_CUDA;
 }
 
