@@ -20,6 +20,11 @@ Pins (checked in tests/test_oracle_*.py without a GPU):
          special cases that reduce to a library matmul; scale linearity;
          Dgrad/Wgrad transposition identities.
   group  E=1 equals dense; empty experts; relabelling invariance.
+  gemm_quant  (the GEMM result quantised into 1x128 E4M3 tiles) products that
+         are exact E4M3 values with a 448 in every tile come back unchanged at
+         scale 1; scale direction under power-of-2 operand scales; the tile
+         amax takes code +-448 and every element lies within half an E4M3 step;
+         an all-zero tile.
 Parity unpinned: the "about 2% error at K=4096 with ~14-bit accumulation"
 figure (no mechanism detail to reproduce it); it is context only.
 """
@@ -27,4 +32,4 @@ figure (no mechanism detail to reproduce it); it is context only.
 from .e4m3 import E4M3_MAX, decode, encode  # noqa: F401
 from .quant import (act_quant, act_quant_t, weight_quant, requant_t,  # noqa: F401
                     dequant_tiles, dequant_blocks, scale_from_amax)
-from .scaled_gemm import gemm, grouped_gemm, slice_partials  # noqa: F401
+from .scaled_gemm import gemm, gemm_quant, grouped_gemm, slice_partials  # noqa: F401

@@ -89,3 +89,27 @@ def grouped_gemm(qa, sa, offsets, qb, sb) -> np.ndarray:
         if r1 > r0:
             C[r0:r1] = gemm(qa[r0:r1], np.asarray(sa)[r0:r1], qb[e], sb[e])
     return C
+
+
+def gemm_quant(qa, sa, qb, sb, b_tile: bool = False, pow2: bool = False):
+    """The GEMM's FP32 result quantised into 1x128 E4M3 tiles along N.
+
+    This is the output an FP8 producer hands to the next FP8 GEMM: the pages
+    cache the inputs of the following Linear as FP8 with per-1x128-tile
+    scales (page 2, inprokorea.com free #735329, fine-grained quantisation
+    passage; power-of-2 scales for the inputs the page names, pages 1 and 2).
+    Reading: the tile is quantised from the float32 rounding of the promoted
+    sum C (no BF16 step in between), with the same amax, scale and multiplier
+    rules as the activation quantiser.
+
+    Returns (q uint8 [M, N], s float32 [M, N/128], x float32 [M, N]) where x is
+    the float32 C that was quantised.
+    """
+    from .quant import act_quant
+
+    C = gemm(qa, sa, qb, sb, b_tile)
+    if C.shape[1] % TILE:
+        raise ValueError("N must be a multiple of 128 for 1x128 output tiles")
+    x = C.astype(np.float32)                         # RNE from float64
+    q, s = act_quant(x, pow2)
+    return q, s, x

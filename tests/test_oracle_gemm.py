@@ -218,3 +218,82 @@ def test_planted_mistakes_are_caught(monkeypatch):
     monkeypatch.setattr(og, "decode", lambda c: -real_decode(c) if np.asarray(c).shape[0] == 2 else real_decode(c))
     with pytest.raises(AssertionError):
         test_bruteforce_rational(3, 2, 256, True)
+
+
+# --------------------------------------------------------------------------
+# The GEMM result quantised into 1x128 E4M3 tiles (the FP8 producer output).
+
+def _exact_e4m3_rows(M, N, g):
+    """A = 1.0 at k=0 only, B row n carries code c_n at k=0: C[m, n] = value(c_n)."""
+    K = 128
+    qa = np.zeros((M, K), np.uint8)
+    qa[:, 0] = 0x38                                   # 1.0
+    codes = g.choice(FINITE, size=N).astype(np.uint8)
+    for t in range(N // 128):
+        codes[128 * t + int(g.integers(0, 128))] = 0x7E  # each tile holds +448
+    qb = np.zeros((N, K), np.uint8)
+    qb[:, 0] = codes
+    return qa, qb, codes
+
+
+@pytest.mark.parametrize("pow2", [False, True])
+def test_gemm_quant_returns_exact_e4m3_products_unchanged(pow2):
+    # every C value is an E4M3 value and each tile's amax is 448, so the scale
+    # is exactly 1 and every code comes back (negative zero sums to +0)
+    g = np.random.default_rng(11)
+    qa, qb, codes = _exact_e4m3_rows(3, 384, g)
+    sa = np.ones((3, 1), np.float32)
+    sb = np.ones((3, 1), np.float32)
+    q, s, x = og.gemm_quant(qa, sa, qb, sb, pow2=pow2)
+    want = np.where(codes == 0x80, 0x00, codes).astype(np.uint8)
+    assert np.all(s == 1.0)
+    for m in range(3):
+        assert np.array_equal(q[m], want)
+
+
+@pytest.mark.parametrize("pow2", [False, True])
+def test_gemm_quant_scale_direction(pow2):
+    # sa = 2^3, sb = 2^-5: C = value * 2^-2, tile amax 112, dequant scale 1/4
+    g = np.random.default_rng(12)
+    qa, qb, codes = _exact_e4m3_rows(2, 256, g)
+    sa = np.full((2, 1), 8.0, np.float32)
+    sb = np.full((2, 1), 2.0 ** -5, np.float32)
+    q, s, x = og.gemm_quant(qa, sa, qb, sb, pow2=pow2)
+    assert np.all(s == 0.25)
+    want = np.where(codes == 0x80, 0x00, codes).astype(np.uint8)
+    assert np.array_equal(q[1], want)
+    assert np.array_equal(e4m3.decode(q[0]) * 0.25, x[0].astype(np.float64))
+
+
+def test_gemm_quant_tile_bound_and_amax_code():
+    # random operands: the tile amax takes code +-448 (non-pow2) and every
+    # element is within half an E4M3 step of x / s
+    g = np.random.default_rng(13)
+    M, N, K = 5, 256, 384
+    qa, qb = _codes((M, K), g), _codes((N, K), g)
+    sa, sb = _scales((M, K // 128), g), _scales((N // 128, K // 128), g)
+    q, s, x = og.gemm_quant(qa, sa, qb, sb)
+    C = og.gemm(qa, sa, qb, sb)
+    assert np.array_equal(x, C.astype(np.float32))
+    for m in range(M):
+        for t in range(N // 128):
+            xt = x[m, 128 * t:128 * (t + 1)].astype(np.float64)
+            qt = q[m, 128 * t:128 * (t + 1)]
+            st = float(s[m, t])
+            i = int(np.argmax(np.abs(xt)))
+            assert e4m3.decode(qt[i:i + 1])[0] == np.copysign(448.0, xt[i])
+            y = xt / st
+            # E4M3 spacing: 2^(e-3) for |y| in [2^e, 2^(e+1)), 2^-9 below 2^-6
+            step = np.where(np.abs(y) < 2.0 ** -6, 2.0 ** -9,
+                            2.0 ** (np.floor(np.log2(np.maximum(np.abs(y), 2.0 ** -6))) - 3))
+            assert np.all(np.abs(e4m3.decode(qt) - y) <= 0.5 * step * (1 + 1e-6))
+
+
+def test_gemm_quant_zero_tile_and_ragged_n():
+    qa = np.zeros((1, 128), np.uint8)
+    qb = np.zeros((128, 128), np.uint8)
+    q, s, _ = og.gemm_quant(qa, np.ones((1, 1), np.float32), qb, np.ones((1, 1), np.float32))
+    assert np.all(q == 0) and s[0, 0] == np.float32(2.0 ** -64) / np.float32(448)
+    with pytest.raises(ValueError):
+        og.gemm_quant(np.zeros((1, 128), np.uint8), np.ones((1, 1), np.float32),
+                      np.zeros((144, 128), np.uint8), np.ones((144, 1), np.float32), b_tile=True)
