@@ -47,7 +47,7 @@ def parse():
     p.add_argument("--gpus", type=int, default=1)
     p.add_argument("--steps", type=int, default=None,
                    help="timed steps (default: 2000 for fprop, 200 for the other workloads)")
-    p.add_argument("--workload", choices=["fprop", "backward", "moe", "ksweep"], default="fprop",
+    p.add_argument("--workload", choices=["fprop", "backward", "moe", "ksweep", "producer"], default="fprop",
                    help="fprop is the headline step; the others time the remaining hot-path "
                         "kernels on their own workloads (one JSON line each)")
     p.add_argument("--warmup", type=int, default=10)
@@ -468,6 +468,37 @@ def run_workload(args, rank, world):
                 "data": "synthetic: tokens N(0,1), router N(0,0.02^2), bias U(-0.1,0.1), experts N(0,0.02^2), "
                         "h = silu(g)*u with g,u N(0,1.7^2)"}
         flops = {"grouped_up": 2 * T * 2 * I * H, "grouped_down": 2 * T * H * I}
+    elif args.workload == "producer":
+        # the Fprop GEMM as the producer of the next FP8 GEMM's input: BF16 out
+        # then act_quant of it, against the fused E4M3 epilogue
+        Mt, Nf, Kh = 4096, 18432, 7168
+        case = synth.dense_case("fprop")
+        x, w = case.x().to(dev), case.w().to(dev)
+        qx, sx = u8(Mt, Kh), f32(Mt, Kh // 128)
+        qw, sw = u8(Nf, Kh), f32(Nf // 128, Kh // 128)
+        check(lib.fp8_act_quant(x.data_ptr(), fp8.BF16, Mt, Kh, qx.data_ptr(), sx.data_ptr(), 0, sp), "act_quant")
+        check(lib.fp8_weight_quant(w.data_ptr(), fp8.BF16, Nf, Kh, qw.data_ptr(), sw.data_ptr(), None, None, 0,
+                                   sp), "weight_quant")
+        yb = torch.empty((Mt, Nf), dtype=torch.bfloat16, device=dev)
+        qy, sy = u8(Mt, Nf), f32(Mt, Nf // 128)
+        qy2, sy2 = u8(Mt, Nf), f32(Mt, Nf // 128)
+        ops += [
+            ("gemm_bf16", lambda: check(lib.fp8_blockscaled_gemm(
+                qx.data_ptr(), sx.data_ptr(), qw.data_ptr(), sw.data_ptr(), yb.data_ptr(), fp8.BF16,
+                Mt, Nf, Kh, 0, sp), "gemm"),
+             "tensor", 2 * Mt * Nf * Kh),
+            ("act_quant_Y", lambda: check(lib.fp8_act_quant(
+                yb.data_ptr(), fp8.BF16, Mt, Nf, qy.data_ptr(), sy.data_ptr(), 0, sp), "act_quant"),
+             "hbm", Mt * Nf * 3 + Mt * Nf // 128 * 4),
+            ("gemm_quant_fused", lambda: check(lib.fp8_blockscaled_gemm_quant(
+                qx.data_ptr(), sx.data_ptr(), qw.data_ptr(), sw.data_ptr(), qy2.data_ptr(), sy2.data_ptr(),
+                Mt, Nf, Kh, 0, sp), "gemm_quant"),
+             "tensor", 2 * Mt * Nf * Kh),
+        ]
+        desc = {"workload": "producer_fprop_x4096x7168_w18432x7168",
+                "step": "unfused: gemm -> bf16 [4096,18432] + act_quant of it; fused: gemm with the 1x128 "
+                        "E4M3 quantisation in its epilogue (both per step; value counts both GEMMs)",
+                "data": "synthetic (seeded N(0,1) X with 0.1% x100 outliers, N(0,0.02) W)"}
     else:  # ksweep
         for Kk in (4096, 8192, 16384):
             cs = synth.dense_case(f"ksweep{Kk}")

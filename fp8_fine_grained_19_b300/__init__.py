@@ -17,7 +17,7 @@ import torch
 
 __all__ = [
     "Fp8Error", "load", "lib_path", "act_quant", "weight_quant", "requant_transpose", "gemm",
-    "grouped_gemm",
+    "gemm_quant", "grouped_gemm",
     "device_status", "set_wait_limit", "selftest_wait_timeout", "status_string",
     "OK", "ERR_INVALID_ARG", "ERR_UNSUPPORTED_SHAPE", "ERR_MISALIGNED", "ERR_CUDA",
     "ERR_TIMEOUT", "ERR_BAD_OFFSETS", "POW2", "TRANSPOSE", "B_TILE1x128", "BF16", "F32",
@@ -37,6 +37,7 @@ _SIGS = {
     "fp8_weight_quant": [_vp, ctypes.c_int, _i64, _i64, _vp, _vp, _vp, _vp, _u32, _vp],
     "fp8_requant_transpose": [_vp, _vp, _i64, _i64, _vp, _vp, _u32, _vp],
     "fp8_blockscaled_gemm": [_vp, _vp, _vp, _vp, _vp, ctypes.c_int, _i64, _i64, _i64, _u32, _vp],
+    "fp8_blockscaled_gemm_quant": [_vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _u32, _vp],
     "fp8_grouped_gemm": [_vp, _vp, _vp, _i32, _i64, _vp, _vp, _vp, ctypes.c_int, _i64, _i64,
                          _u32, _vp],
     "fp8_get_device_status": [_vp],
@@ -183,6 +184,30 @@ def gemm(a, sa, b, sb, out_dtype=torch.bfloat16, b_tile: bool = False, out=None,
                                        B_TILE1x128 if b_tile else 0, _stream(stream)),
            "fp8_blockscaled_gemm")
     return out
+
+
+def gemm_quant(a, sa, b, sb, b_tile: bool = False, pow2: bool = False, out=None,
+               out_scales=None, stream=None):
+    """The gemm result quantised in the epilogue: (q uint8 [M, N], s float32 [M, N/128])."""
+    for t, n in ((a, "a"), (b, "b")):
+        _need(t, (torch.uint8,), n)
+    for t, n in ((sa, "sa"), (sb, "sb")):
+        _need(t, (torch.float32,), n)
+    M, K = a.shape
+    N = b.shape[0]
+    if b.shape[1] != K:
+        raise ValueError("a and b disagree on K")
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.uint8, device=a.device)
+    if out_scales is None:
+        out_scales = torch.empty((M, max(N // 128, 1)), dtype=torch.float32, device=a.device)
+    _need(out, (torch.uint8,), "out")
+    _need(out_scales, (torch.float32,), "out_scales")
+    flags = (B_TILE1x128 if b_tile else 0) | (POW2 if pow2 else 0)
+    _check(load().fp8_blockscaled_gemm_quant(_ptr(a), _ptr(sa), _ptr(b), _ptr(sb), _ptr(out),
+                                             _ptr(out_scales), M, N, K, flags, _stream(stream)),
+           "fp8_blockscaled_gemm_quant")
+    return out, out_scales
 
 
 def grouped_gemm(a, sa, offsets, b, sb, out_dtype=torch.bfloat16, out=None, stream=None):

@@ -133,7 +133,7 @@ bool have_device() { return device_sm_count() > 0; }
 
 extern "C" {
 
-int fp8fg_abi_version(void) { return 2; }
+int fp8fg_abi_version(void) { return 3; }
 
 const char* fp8fg_status_string(fp8fg_status status) {
   switch (status) {
@@ -215,6 +215,28 @@ fp8fg_status fp8_blockscaled_gemm(const uint8_t* a, const float* sa, const uint8
   if (M == 0) return FP8FG_OK;
   if (!have_device()) return FP8FG_ERR_CUDA;
   return launch_gemm(a, sa, b, sb, c, c_dtype, M, N, K, b_tile, as_stream(stream));
+}
+
+fp8fg_status fp8_blockscaled_gemm_quant(const uint8_t* a, const float* sa, const uint8_t* b,
+                                        const float* sb, uint8_t* q, float* s, int64_t M,
+                                        int64_t N, int64_t K, unsigned flags, void* stream) {
+  if ((flags & ~(FP8FG_B_TILE1x128 | FP8FG_POW2)) != 0 || M < 0 || N < 0 || K < 0)
+    return FP8FG_ERR_INVALID_ARG;
+  if (b == nullptr || sb == nullptr || (M > 0 && (a == nullptr || sa == nullptr || q == nullptr ||
+                                                  s == nullptr)))
+    return FP8FG_ERR_INVALID_ARG;
+  const bool b_tile = (flags & FP8FG_B_TILE1x128) != 0;
+  if (K < 128 || K % 128 != 0 || N < 128 || N % 128 != 0 || M > kMaxDim || N > kMaxDim ||
+      K > kMaxDim)
+    return FP8FG_ERR_UNSUPPORTED_SHAPE;
+  if (((M + 127) / 128) * ((N + 255) / 256) > kMaxDim) return FP8FG_ERR_UNSUPPORTED_SHAPE;
+  if (!aligned16(a) || !aligned16(sa) || !aligned16(b) || !aligned16(sb) || !aligned16(q) ||
+      !aligned16(s))
+    return FP8FG_ERR_MISALIGNED;
+  if (M == 0) return FP8FG_OK;
+  if (!have_device()) return FP8FG_ERR_CUDA;
+  return launch_gemm_quant(a, sa, b, sb, q, s, M, N, K, b_tile, (flags & FP8FG_POW2) != 0,
+                           as_stream(stream));
 }
 
 fp8fg_status fp8_grouped_gemm(const uint8_t* a, const float* sa, const int32_t* offsets, int32_t E,

@@ -256,6 +256,32 @@ __device__ __forceinline__ uint64_t mul2(uint64_t a, uint64_t b) {
   return d;
 }
 
+// ------------------------------------------------------- E4M3 tile scales
+// Scale rule of every 1x128 tile / 128x128 block (page 2, inprokorea.com free
+// #735329, online-amax passage; pages 1-2, power-of-2 passage): amax floored
+// at 2^-64; dequantisation scale s = amax/448 and multiplier m = 448/amax by
+// IEEE division, or in power-of-2 mode s = 2^ceil(log2(amax/448)) and m = 1/s
+// built from the exponent bits.  Codes are e4m3(x * m) with one IEEE multiply.
+constexpr float kE4M3Max = 448.0f;
+constexpr float kAmaxFloor = 5.42101086242752217e-20f;  // 2^-64
+
+struct Scale {
+  float s;  // dequantisation scale (stored)
+  float m;  // quantisation multiplier
+};
+
+__device__ __forceinline__ Scale scale_from_amax(float amax, bool pow2) {
+  const float a = fmaxf(amax, kAmaxFloor);
+  const float t = __fdiv_rn(a, kE4M3Max);
+  if (!pow2) return {t, __fdiv_rn(kE4M3Max, a)};
+  // t is a normal float in [2^-73, 2^120]: round up to the next power of two
+  const uint32_t bits = __float_as_uint(t);
+  int e = static_cast<int>((bits >> 23) & 0xFF) - 127;
+  if (bits & 0x7FFFFFu) e += 1;
+  return {__uint_as_float(static_cast<uint32_t>(e + 127) << 23),
+          __uint_as_float(static_cast<uint32_t>(127 - e) << 23)};
+}
+
 // Two floats -> two E4M3 codes (RNE, saturating); `lo` lands in the low byte.
 __device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {
   uint16_t r;

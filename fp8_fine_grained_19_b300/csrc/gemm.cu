@@ -82,6 +82,8 @@ struct GemmParams {
   int E;
   int c_f32;
   int b_tile;
+  float* s_out;           // quantised output: [rows, N/128] tile scales
+  int pow2_out;           // quantised output: power-of-2 scales
   long long wait_limit;
   int* status;            // library status word
 };
@@ -160,7 +162,7 @@ __device__ __forceinline__ Tile tile_of(int t, const GemmParams& p, const Smem& 
   return r;
 }
 
-template <bool GROUPED, bool BTILE>
+template <bool GROUPED, bool BTILE, bool OUTQ>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     blockscaled_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                             const __grid_constant__ CUtensorMap tmB,
@@ -474,6 +476,56 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             }
           }
         }
+      } else if constexpr (OUTQ) {
+        // --- dense, E4M3 output: the thread's 128 columns of its row are one
+        // 1x128 tile; the same amax/scale/multiplier rules as act_quant apply
+        // to the FP32 accumulator, and the codes leave like the BF16 output
+        // (two 64-byte chunks per row through the swizzled staging).
+        const int wrow0 = tl.m0 + quad * 32;
+        if (half_ok && wrow0 < p.M) {
+          float amax = 0.0f;
+#pragma unroll
+          for (int j = 0; j < 64; ++j) {
+            float lo, hi;
+            unpack2(acc[j], lo, hi);
+            amax = fmaxf(amax, fmaxf(fabsf(lo), fabsf(hi)));
+          }
+          const Scale sc = scale_from_amax(amax, p.pow2_out != 0);
+          if (row < p.M) p.s_out[static_cast<int64_t>(row) * (p.N / 128) + col_h / 128] = sc.s;
+          uint32_t wl = (warp << 8) | lane;
+          asm volatile("" : "+r"(wl));
+          const uint32_t cbuf = smem_u32(sm.cst[0]) + (wl >> 8) * CST_BYTES;
+          const uint32_t srow = cbuf + (wl & 31) * CST_ROW;
+          const uint32_t swz = ((wl & 31) >> 1) & 3;
+#pragma unroll
+          for (int q = 0; q < 2; ++q) {           // 64 codes per chunk
+            if (staged) {
+              if (lane == 0) bulk_wait_read_all();
+              __syncwarp();
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              uint32_t w[4];
+#pragma unroll
+              for (int i = 0; i < 4; ++i) {
+                // columns 64q + 16u + 4i .. +3 = accumulator pairs 32q + 8u + 2i, +1
+                float x0, x1, x2, x3;
+                unpack2(acc[32 * q + 8 * u + 2 * i], x0, x1);
+                unpack2(acc[32 * q + 8 * u + 2 * i + 1], x2, x3);
+                w[i] = e4m3x2(__fmul_rn(x0, sc.m), __fmul_rn(x1, sc.m)) |
+                       (e4m3x2(__fmul_rn(x2, sc.m), __fmul_rn(x3, sc.m)) << 16);
+              }
+              sts_128(srow + ((u ^ swz) << 4), w[0], w[1], w[2], w[3]);
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              tma_store_2d(&tmC, cbuf, col_h + 64 * q, wrow0);
+              bulk_commit();
+            }
+            staged = true;
+          }
+        }
       } else {
         // --- dense: the warp's 32 rows x 128 columns of its half go out in
         // chunks of 64 bytes per row.  Chunk q of row `lane` goes to staging
@@ -597,10 +649,10 @@ bool make_c_map(CUtensorMap* mC, void* c, fp8fg_dtype ct, int64_t rows, int64_t 
                            c, 2, dC, sC, boxC, CU_TENSOR_MAP_SWIZZLE_64B);
 }
 
-template <bool GROUPED, bool BTILE>
+template <bool GROUPED, bool BTILE, bool OUTQ = false>
 cudaError_t set_smem_attr() {
   static const cudaError_t e = cudaFuncSetAttribute(
-      blockscaled_gemm_kernel<GROUPED, BTILE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+      blockscaled_gemm_kernel<GROUPED, BTILE, OUTQ>, cudaFuncAttributeMaxDynamicSharedMemorySize,
       static_cast<int>(kSmemBytes));
   return e;
 }
@@ -634,9 +686,51 @@ fp8fg_status launch_gemm(const uint8_t* a, const float* sa, const uint8_t* b, co
   const int tiles = p.m_tiles * p.n_tiles;
   const int grid = tiles < device_sm_count() ? tiles : device_sm_count();
   if (b_tile)
-    blockscaled_gemm_kernel<false, true><<<grid, NUM_THREADS, kSmemBytes, st>>>(mA, mB, mC, p);
+    blockscaled_gemm_kernel<false, true, false><<<grid, NUM_THREADS, kSmemBytes, st>>>(mA, mB, mC, p);
   else
-    blockscaled_gemm_kernel<false, false><<<grid, NUM_THREADS, kSmemBytes, st>>>(mA, mB, mC, p);
+    blockscaled_gemm_kernel<false, false, false><<<grid, NUM_THREADS, kSmemBytes, st>>>(mA, mB, mC, p);
+  return cudaGetLastError() == cudaSuccess ? FP8FG_OK : FP8FG_ERR_CUDA;
+}
+
+fp8fg_status launch_gemm_quant(const uint8_t* a, const float* sa, const uint8_t* b,
+                               const float* sb, uint8_t* q, float* s, int64_t M, int64_t N,
+                               int64_t K, bool b_tile, bool pow2, cudaStream_t st) {
+  CUtensorMap mA, mB, mQ;
+  if (!make_maps(&mA, &mB, a, M, b, 0, N, K)) return FP8FG_ERR_CUDA;
+  // codes [M, N] stored by 32-row x 64-byte boxes from 64-byte-swizzled staging
+  const uint64_t dQ[2] = {static_cast<uint64_t>(N), static_cast<uint64_t>(M)};
+  const uint64_t sQ[1] = {static_cast<uint64_t>(N)};
+  const uint32_t boxQ[2] = {CST_ROW, 32};
+  if (!encode_tensor_map(&mQ, CU_TENSOR_MAP_DATA_TYPE_UINT8, q, 2, dQ, sQ, boxQ,
+                         CU_TENSOR_MAP_SWIZZLE_64B))
+    return FP8FG_ERR_CUDA;
+  if ((b_tile ? set_smem_attr<false, true, true>() : set_smem_attr<false, false, true>()) !=
+      cudaSuccess)
+    return FP8FG_ERR_CUDA;
+  GemmParams p{};
+  p.sa = sa;
+  p.sb = sb;
+  p.c = q;
+  p.offsets = nullptr;
+  p.M = static_cast<int>(M);
+  p.N = static_cast<int>(N);
+  p.K = static_cast<int>(K);
+  p.nkb = static_cast<int>(K / BK);
+  p.m_tiles = static_cast<int>((M + BM - 1) / BM);
+  p.n_tiles = static_cast<int>((N + BN - 1) / BN);
+  p.E = 1;
+  p.c_f32 = 0;
+  p.b_tile = b_tile ? 1 : 0;
+  p.s_out = s;
+  p.pow2_out = pow2 ? 1 : 0;
+  p.wait_limit = wait_limit_cycles();
+  p.status = device_status_word();
+  const int tiles = p.m_tiles * p.n_tiles;
+  const int grid = tiles < device_sm_count() ? tiles : device_sm_count();
+  if (b_tile)
+    blockscaled_gemm_kernel<false, true, true><<<grid, NUM_THREADS, kSmemBytes, st>>>(mA, mB, mQ, p);
+  else
+    blockscaled_gemm_kernel<false, false, true><<<grid, NUM_THREADS, kSmemBytes, st>>>(mA, mB, mQ, p);
   return cudaGetLastError() == cudaSuccess ? FP8FG_OK : FP8FG_ERR_CUDA;
 }
 
@@ -665,8 +759,8 @@ fp8fg_status launch_grouped_gemm(const uint8_t* a, const float* sa, const int32_
   p.b_tile = 0;
   p.wait_limit = wait_limit_cycles();
   p.status = device_status_word();
-  blockscaled_gemm_kernel<true, false><<<device_sm_count(), NUM_THREADS, kSmemBytes, st>>>(mA, mB,
-                                                                                          mC, p);
+  blockscaled_gemm_kernel<true, false, false><<<device_sm_count(), NUM_THREADS, kSmemBytes, st>>>(
+      mA, mB, mC, p);
   return cudaGetLastError() == cudaSuccess ? FP8FG_OK : FP8FG_ERR_CUDA;
 }
 

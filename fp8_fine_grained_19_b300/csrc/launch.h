@@ -29,6 +29,10 @@ cudaError_t launch_weight_quant(const void* w, fp8fg_dtype wt, int64_t N, int64_
 fp8fg_status launch_gemm(const uint8_t* a, const float* sa, const uint8_t* b, const float* sb,
                          void* c, fp8fg_dtype ct, int64_t M, int64_t N, int64_t K, bool b_tile,
                          cudaStream_t st);
+// Dense block-scaled GEMM whose result leaves as 1x128 E4M3 tiles (q, s).
+fp8fg_status launch_gemm_quant(const uint8_t* a, const float* sa, const uint8_t* b,
+                               const float* sb, uint8_t* q, float* s, int64_t M, int64_t N,
+                               int64_t K, bool b_tile, bool pow2, cudaStream_t st);
 // Grouped block-scaled GEMM over contiguous expert row groups.
 fp8fg_status launch_grouped_gemm(const uint8_t* a, const float* sa, const int32_t* offsets,
                                  int32_t E, int64_t total_rows, const uint8_t* b, const float* sb,

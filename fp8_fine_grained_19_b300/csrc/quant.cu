@@ -25,26 +25,6 @@ namespace fp8fg {
 
 namespace {
 
-constexpr float kE4M3Max = 448.0f;
-constexpr float kAmaxFloor = 5.42101086242752217e-20f;  // 2^-64
-
-struct Scale {
-  float s;  // dequantisation scale (stored)
-  float m;  // quantisation multiplier
-};
-
-__device__ __forceinline__ Scale scale_from_amax(float amax, bool pow2) {
-  const float a = fmaxf(amax, kAmaxFloor);
-  const float t = __fdiv_rn(a, kE4M3Max);
-  if (!pow2) return {t, __fdiv_rn(kE4M3Max, a)};
-  // t is a normal float in [2^-73, 2^120]: round up to the next power of two
-  const uint32_t bits = __float_as_uint(t);
-  int e = static_cast<int>((bits >> 23) & 0xFF) - 127;
-  if (bits & 0x7FFFFFu) e += 1;
-  return {__uint_as_float(static_cast<uint32_t>(e + 127) << 23),
-          __uint_as_float(static_cast<uint32_t>(127 - e) << 23)};
-}
-
 // 16-byte streaming load (read once; do not keep in L1).
 __device__ __forceinline__ uint4 ld_stream16(const void* p) {
   uint4 v;
@@ -79,9 +59,6 @@ struct Vec16<float> {
     f[3] = __uint_as_float(v.w);
   }
 };
-
-__device__ __forceinline__ float to_f32(__nv_bfloat16 v) { return __bfloat162float(v); }
-__device__ __forceinline__ float to_f32(float v) { return v; }
 
 // --------------------------------------------------------------------------
 // 1x128 tiles along K.  With K % 128 == 0 the tiles of a row-major [M, K]

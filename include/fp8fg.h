@@ -132,6 +132,28 @@ fp8fg_status fp8_blockscaled_gemm(const uint8_t* a, const float* sa, const uint8
                                   int64_t N, int64_t K, unsigned flags, void* stream);
 
 /*
+ * fp8_blockscaled_gemm_quant -- fp8_blockscaled_gemm whose FP32 result is
+ * quantised in the epilogue into 1x128 E4M3 tiles along N, the form in which
+ * the next FP8 GEMM takes its activation input.  Source: page 2, fine-grained
+ * quantisation passage (1x128 activation tiles, online amax, FP32 scales);
+ * pages 1-2, power-of-2 passage (integral power-of-2 scales for the inputs the
+ * pages name).  Reading: the tile is quantised from the FP32 accumulator, with
+ * no BF16 rounding in between.
+ *
+ * a, sa, b, sb as fp8_blockscaled_gemm (flags may hold FP8FG_B_TILE1x128).
+ * q  [M, N] E4M3 codes, row-major; s [M, N/128] FP32 dequantisation scales.
+ * Per tile: amax = max |C| floored at 2^-64; s = amax/448 and codes
+ * e4m3(C * (448/amax)) (IEEE division and multiply, RNE, saturating), or with
+ * FP8FG_POW2 s = 2^ceil(log2(amax/448)) and codes e4m3(C / s).  Equal to
+ * fp8_act_quant applied to the FP32 output of fp8_blockscaled_gemm.
+ * Requires N % 128 == 0, K % 128 == 0, K >= 128; M >= 0 (0: nothing launched).
+ * Pointers 16-byte aligned; the caller owns all memory.
+ */
+fp8fg_status fp8_blockscaled_gemm_quant(const uint8_t* a, const float* sa, const uint8_t* b,
+                                        const float* sb, uint8_t* q, float* s, int64_t M,
+                                        int64_t N, int64_t K, unsigned flags, void* stream);
+
+/*
  * fp8_grouped_gemm -- fp8_blockscaled_gemm per routed expert over contiguous
  * row groups.  Source: page 2, passage quantising the activation before the
  * MoE up-projection for FP8 Fprop; page 5, MoE configuration passage (256

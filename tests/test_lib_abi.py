@@ -40,7 +40,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_abi_version_and_status_strings(lib):
-    assert lib.fp8fg_abi_version() == 2
+    assert lib.fp8fg_abi_version() == 3
     for code in range(7):
         assert fp8.status_string(code)
     assert "unknown" in fp8.status_string(99)
@@ -97,6 +97,18 @@ def test_gemm_rejections(lib):
     assert f(*ok, 0, 128, 200, 256, fp8.B_TILE1x128, None) == fp8.ERR_UNSUPPORTED_SHAPE  # N % 16
     assert f(A16, A16, MIS, A16, A16, 0, 128, 256, 256, 0, None) == fp8.ERR_MISALIGNED
     assert f(None, None, A16, A16, None, 0, 0, 256, 256, 0, None) == fp8.OK             # M == 0
+
+
+def test_gemm_quant_rejections(lib):
+    f = lib.fp8_blockscaled_gemm_quant
+    ok = (A16, A16, A16, A16, A16, A16)
+    assert f(*ok, 128, 256, 256, 2, None) == fp8.ERR_INVALID_ARG                      # TRANSPOSE
+    assert f(*ok, 128, 256, 256, 8, None) == fp8.ERR_INVALID_ARG                      # unknown
+    assert f(A16, A16, A16, A16, A16, None, 128, 256, 256, 0, None) == fp8.ERR_INVALID_ARG
+    assert f(*ok, 128, 256, 200, 0, None) == fp8.ERR_UNSUPPORTED_SHAPE                # K % 128
+    assert f(*ok, 128, 144, 256, fp8.B_TILE1x128, None) == fp8.ERR_UNSUPPORTED_SHAPE  # N % 128
+    assert f(A16, A16, A16, A16, A16, MIS, 128, 256, 256, 0, None) == fp8.ERR_MISALIGNED
+    assert f(None, None, A16, A16, None, None, 0, 256, 256, fp8.POW2, None) == fp8.OK  # M == 0
 
 
 def test_grouped_rejections(lib):
