@@ -25,6 +25,11 @@ Pins (checked in tests/test_oracle_*.py without a GPU):
          scale 1; scale direction under power-of-2 operand scales; the tile
          amax takes code +-448 and every element lies within half an E4M3 step;
          an all-zero tile.
+  swiglu silu against scipy's logistic and the odd identity
+         silu(x) - silu(-x) = x; a worked case where silu(64) = 64 exactly makes
+         h = 64 * up and the up codes come back under scale 64; swapping the
+         gate and up halves changes the result; power-of-2 scales and the
+         half-step bound on random tiles.
 Parity unpinned: the "about 2% error at K=4096 with ~14-bit accumulation"
 figure (no mechanism detail to reproduce it); it is context only.
 """
@@ -32,4 +37,5 @@ figure (no mechanism detail to reproduce it); it is context only.
 from .e4m3 import E4M3_MAX, decode, encode  # noqa: F401
 from .quant import (act_quant, act_quant_t, weight_quant, requant_t,  # noqa: F401
                     dequant_tiles, dequant_blocks, scale_from_amax)
-from .scaled_gemm import gemm, gemm_quant, grouped_gemm, slice_partials  # noqa: F401
+from .scaled_gemm import (gemm, gemm_quant, grouped_gemm, grouped_swiglu_quant,  # noqa: F401
+                          silu, slice_partials)

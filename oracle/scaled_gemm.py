@@ -113,3 +113,36 @@ def gemm_quant(qa, sa, qb, sb, b_tile: bool = False, pow2: bool = False):
     x = C.astype(np.float32)                         # RNE from float64
     q, s = act_quant(x, pow2)
     return q, s, x
+
+
+def silu(g):
+    """g * sigmoid(g) = g / (1 + exp(-g)) in float64."""
+    g = np.asarray(g, dtype=np.float64)
+    with np.errstate(over="ignore"):
+        return g / (1.0 + np.exp(-g))
+
+
+def grouped_swiglu_quant(qa, sa, offsets, qb, sb, pow2: bool = True):
+    """Routed up-projection followed by SwiGLU, quantised as the down-projection input.
+
+    qb [E, 2I, K] holds each expert's gate rows (0..I-1) then up rows (I..2I-1);
+    with C = grouped_gemm(...) [T, 2I], g = C[:, :I], u = C[:, I:]:
+        h = silu(g) * u                      (float64 from the exact sums)
+    then h rounded to float32 and quantised into 1x128 tiles along I with
+    power-of-2 scales: the down-projection input, which page 2 (inprokorea.com
+    free #735329, power-of-2 passage) and page 1 name among the activations
+    cached in FP8 with integral power-of-2 scales.  The SwiGLU form and the
+    gate/up row order are readings (the pages name neither).
+
+    Returns (q uint8 [T, I], s float32 [T, I/128], h float32 [T, I]).
+    """
+    from .quant import act_quant
+
+    qb = np.asarray(qb)
+    if qb.shape[1] % 256:
+        raise ValueError("2I must be a multiple of 256")
+    C = grouped_gemm(qa, sa, offsets, qb, sb)
+    I = qb.shape[1] // 2
+    h = (silu(C[:, :I]) * C[:, I:]).astype(np.float32)
+    q, s = act_quant(h, pow2)
+    return q, s, h

@@ -297,3 +297,86 @@ def test_gemm_quant_zero_tile_and_ragged_n():
     with pytest.raises(ValueError):
         og.gemm_quant(np.zeros((1, 128), np.uint8), np.ones((1, 1), np.float32),
                       np.zeros((144, 128), np.uint8), np.ones((144, 1), np.float32), b_tile=True)
+
+
+# --------------------------------------------------------------------------
+# Routed up-projection + SwiGLU, quantised as the down-projection input.
+
+def test_silu_against_library_logistic_and_odd_identity():
+    from scipy.special import expit
+    x = np.concatenate([np.linspace(-40, 40, 801), [0.0, 1e-30, -1e-30, 700.0, -700.0]])
+    assert np.allclose(og.silu(x), x * expit(x), rtol=1e-14, atol=0)
+    # sigmoid(x) + sigmoid(-x) = 1  =>  silu(x) - silu(-x) = x
+    assert np.allclose(og.silu(x) - og.silu(-x), x, rtol=1e-14, atol=1e-300)
+    assert og.silu(0.0) == 0.0 and og.silu(64.0) == 64.0
+
+
+def _swiglu_case(rows_per_expert, I, g):
+    """Gate = 64 exactly for every row, up = E4M3 values: h = 64 * value(up code)."""
+    E = len(rows_per_expert)
+    T = int(sum(rows_per_expert))
+    K = 128
+    qa = np.zeros((T, K), np.uint8)
+    qa[:, 0] = 0x38                                    # 1.0
+    qb = np.zeros((E, 2 * I, K), np.uint8)
+    ups = []
+    for e in range(E):
+        codes = g.choice(FINITE, size=I).astype(np.uint8)
+        for t in range(I // 128):
+            codes[128 * t + int(g.integers(0, 128))] = 0x7E   # 448 in every tile
+        qb[e, :I, 0] = 0x68                            # gate row value 64
+        qb[e, I:, 0] = codes                           # up row values
+        ups.append(codes)
+    off = np.concatenate([[0], np.cumsum(rows_per_expert)]).astype(np.int64)
+    sa = np.ones((T, 1), np.float32)
+    sb = np.ones((E, 2 * I // 128, 1), np.float32)
+    return qa, sa, off, qb, sb, ups
+
+
+def test_swiglu_quant_worked_exact_case():
+    # silu(64) = 64 exactly in float64, so h = 64 * up; every tile's amax is
+    # 64 * 448 and its power-of-2 scale 64: the up codes come back unchanged
+    g = np.random.default_rng(21)
+    qa, sa, off, qb, sb, ups = _swiglu_case([3, 0, 5], 256, g)
+    q, s, h = og.grouped_swiglu_quant(qa, sa, off, qb, sb)
+    assert np.all(s == 64.0)
+    for e, (r0, r1) in enumerate(zip(off[:-1], off[1:])):
+        want = np.where(ups[e] == 0x80, 0, ups[e]).astype(np.uint8)
+        for r in range(r0, r1):
+            assert np.array_equal(q[r], want)
+            assert np.array_equal(h[r], (64.0 * e4m3.decode(want)).astype(np.float32))
+
+
+def test_swiglu_quant_gate_up_order_matters():
+    # swapping the gate and up halves gives silu(up) * 64, not 64 * up
+    g = np.random.default_rng(22)
+    qa, sa, off, qb, sb, ups = _swiglu_case([4], 128, g)
+    swapped = np.concatenate([qb[:, 128:], qb[:, :128]], axis=1)
+    _, _, h = og.grouped_swiglu_quant(qa, sa, off, qb, sb)
+    _, _, h2 = og.grouped_swiglu_quant(qa, sa, off, swapped, sb)
+    assert not np.allclose(h, h2)
+    up = e4m3.decode(ups[0]).astype(np.float64)
+    assert np.allclose(h2[0], (og.silu(up) * 64.0).astype(np.float32))
+
+
+def test_swiglu_quant_random_tiles_bound():
+    # random operands: power-of-2 scales, every element within half an E4M3
+    # step of h / s, and each tile's largest magnitude at most 448 after scaling
+    g = np.random.default_rng(23)
+    sizes = [7, 0, 130, 2]
+    T, I, K = sum(sizes), 256, 256
+    qa = _codes((T, K), g)
+    qb = _codes((len(sizes), 2 * I, K), g)
+    sa = _scales((T, K // 128), g) * 1e-6
+    sb = (_scales((len(sizes), 2 * I // 128, K // 128), g) * 1e-6).astype(np.float32)
+    off = np.concatenate([[0], np.cumsum(sizes)])
+    q, s, h = og.grouped_swiglu_quant(qa, sa.astype(np.float32), off, qb, sb)
+    C = og.grouped_gemm(qa, sa.astype(np.float32), off, qb, sb)
+    assert np.array_equal(h, (og.silu(C[:, :I]) * C[:, I:]).astype(np.float32))
+    assert np.all(np.log2(s) == np.round(np.log2(s)))
+    y = h.astype(np.float64).reshape(T, I // 128, 128) / s[:, :, None]
+    assert np.all(np.abs(y) <= 448.0)
+    dec = e4m3.decode(q).reshape(T, I // 128, 128)
+    step = np.where(np.abs(y) < 2.0 ** -6, 2.0 ** -9,
+                    2.0 ** (np.floor(np.log2(np.maximum(np.abs(y), 2.0 ** -6))) - 3))
+    assert np.all(np.abs(dec - y) <= 0.5 * step * (1 + 1e-9))
