@@ -434,7 +434,6 @@ def run_workload(args, rank, world):
             q_e, s_e = fp8.weight_quant(synth.expert_weight(case, e, "down", dev))
             qdn[e].copy_(q_e)
             sdn[e].copy_(s_e)
-        h = synth.swiglu_like_bf16((T, I), case.seed).to(dev)
         qt, st = u8(case.T, H), f32(case.T, H // 128)
         qh, sh = u8(T, I), f32(T, I // 128)
         up = torch.empty((T, 2 * I), dtype=torch.bfloat16, device=dev)
@@ -444,30 +443,44 @@ def run_workload(args, rank, world):
         # dispatch (row gather in expert order) is routing glue: done once, outside the timed step
         qa, sa = qt.index_select(0, idx).contiguous(), st.index_select(0, idx).contiguous()
         torch.cuda.synchronize()
+        up_bytes = E * 2 * I * H + E * (2 * I // 128) * (H // 128) * 4 + T * H + T * H // 128 * 4
         ops += [
             ("act_quant_tokens_pow2", lambda: check(lib.fp8_act_quant(
                 tok.data_ptr(), fp8.BF16, case.T, H, qt.data_ptr(), st.data_ptr(), fp8.POW2, sp), "act_quant"),
              "hbm", case.T * H * 3 + case.T * H // 128 * 4),
-            ("grouped_up", lambda: check(lib.fp8_grouped_gemm(
-                qa.data_ptr(), sa.data_ptr(), off.data_ptr(), E, T, qu.data_ptr(), su.data_ptr(), up.data_ptr(),
-                fp8.BF16, 2 * I, H, 0, sp), "grouped_up"),
-             "hbm", E * 2 * I * H + E * (2 * I // 128) * (H // 128) * 4 + T * H + T * H // 128 * 4 + T * 2 * I * 2),
-            ("act_quant_h_pow2", lambda: check(lib.fp8_act_quant(
-                h.data_ptr(), fp8.BF16, T, I, qh.data_ptr(), sh.data_ptr(), fp8.POW2, sp), "act_quant"),
-             "hbm", T * I * 3 + T * I // 128 * 4),
+            ("grouped_up_swiglu", lambda: check(lib.fp8_grouped_gemm_swiglu_quant(
+                qa.data_ptr(), sa.data_ptr(), off.data_ptr(), E, T, qu.data_ptr(), su.data_ptr(), qh.data_ptr(),
+                sh.data_ptr(), 2 * I, H, fp8.POW2, sp), "grouped_up_swiglu"),
+             "hbm", up_bytes + T * I + T * I // 128 * 4),
             ("grouped_down", lambda: check(lib.fp8_grouped_gemm(
                 qh.data_ptr(), sh.data_ptr(), off.data_ptr(), E, T, qdn.data_ptr(), sdn.data_ptr(), down.data_ptr(),
                 fp8.BF16, H, I, 0, sp), "grouped_down"),
              "hbm", E * H * I + E * (H // 128) * (I // 128) * 4 + T * I + T * I // 128 * 4 + T * H * 2),
         ]
+        # the unfused producer of the down-projection input, timed apart for comparison
+        h_bf16 = synth.swiglu_like_bf16((T, I), case.seed).to(dev)
+        qh2, sh2 = u8(T, I), f32(T, I // 128)
+        compare_ops = [
+            ("unfused_grouped_up_bf16", lambda: check(lib.fp8_grouped_gemm(
+                qa.data_ptr(), sa.data_ptr(), off.data_ptr(), E, T, qu.data_ptr(), su.data_ptr(), up.data_ptr(),
+                fp8.BF16, 2 * I, H, 0, sp), "grouped_up"),
+             "hbm", up_bytes + T * 2 * I * 2),
+            ("unfused_act_quant_h_pow2", lambda: check(lib.fp8_act_quant(
+                h_bf16.data_ptr(), fp8.BF16, T, I, qh2.data_ptr(), sh2.data_ptr(), fp8.POW2, sp), "act_quant"),
+             "hbm", T * I * 3 + T * I // 128 * 4),
+        ]
         desc = {"workload": "moe_8192tok_h7168_e256_top8_inter2048",
-                "step": "act_quant tokens (pow2) + grouped up-proj [65536,7168]x[256,4096,7168] -> bf16 "
-                        "+ act_quant h (pow2) + grouped down-proj [65536,2048]x[256,7168,2048] -> bf16",
+                "step": "act_quant tokens (pow2) + grouped up-proj [65536,7168]x[256,4096,7168] with SwiGLU and "
+                        "pow2 1x128 quantisation of h in its epilogue + grouped down-proj [65536,2048]x"
+                        "[256,7168,2048] -> bf16",
                 "routing": f"sigmoid + bias top-8 on the host; rows per expert {int(r['counts'].min())}.."
                            f"{int(r['counts'].max())}; row gather done once outside the timed step",
-                "data": "synthetic: tokens N(0,1), router N(0,0.02^2), bias U(-0.1,0.1), experts N(0,0.02^2), "
-                        "h = silu(g)*u with g,u N(0,1.7^2)"}
-        flops = {"grouped_up": 2 * T * 2 * I * H, "grouped_down": 2 * T * H * I}
+                "data": "synthetic: tokens N(0,1), router N(0,0.02^2), bias U(-0.1,0.1), experts N(0,0.02^2); "
+                        "the down-projection input is the fused up-projection's h",
+                "compare": "unfused producer (grouped up -> bf16, then act_quant of an h-shaped bf16 tensor) "
+                           "timed in a separate loop: per_op unfused_*"}
+        flops = {"grouped_up_swiglu": 2 * T * 2 * I * H, "grouped_down": 2 * T * H * I,
+                 "unfused_grouped_up_bf16": 2 * T * 2 * I * H}
     elif args.workload == "producer":
         # the Fprop GEMM as the producer of the next FP8 GEMM's input: BF16 out
         # then act_quant of it, against the fused E4M3 epilogue
@@ -530,14 +543,20 @@ def run_workload(args, rank, world):
 
     steps = args.steps
     total_ms, per, clocks = _timed_loop([(n, f) for n, f, _, _ in ops], steps, args.warmup, stream, dev)
+    extra = []
+    if args.workload == "moe":
+        _, per_c, _ = _timed_loop([(n, f) for n, f, _, _ in compare_ops], max(steps // 4, 5), args.warmup,
+                                  stream, dev)
+        per.update(per_c)
+        extra = compare_ops
     status = fp8.device_status()
     if status != fp8.OK:
         raise RuntimeError(f"device status {fp8.status_string(status)}")
     gemm_flops = sum(a for _, _, k, a in ops if k == "tensor")
     if args.workload == "moe":
-        gemm_flops = sum(flops.values())
+        gemm_flops = flops["grouped_up_swiglu"] + flops["grouped_down"]
     per_op = {}
-    for name, _, kind, amount in ops:
+    for name, _, kind, amount in ops + extra:
         ms = per[name]
         if kind == "tensor":
             tf = amount / (ms * 1e-3) / 1e12

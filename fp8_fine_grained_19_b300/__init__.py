@@ -17,7 +17,7 @@ import torch
 
 __all__ = [
     "Fp8Error", "load", "lib_path", "act_quant", "weight_quant", "requant_transpose", "gemm",
-    "gemm_quant", "grouped_gemm",
+    "gemm_quant", "grouped_gemm", "grouped_swiglu_quant",
     "device_status", "set_wait_limit", "selftest_wait_timeout", "status_string",
     "OK", "ERR_INVALID_ARG", "ERR_UNSUPPORTED_SHAPE", "ERR_MISALIGNED", "ERR_CUDA",
     "ERR_TIMEOUT", "ERR_BAD_OFFSETS", "POW2", "TRANSPOSE", "B_TILE1x128", "BF16", "F32",
@@ -40,6 +40,8 @@ _SIGS = {
     "fp8_blockscaled_gemm_quant": [_vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _u32, _vp],
     "fp8_grouped_gemm": [_vp, _vp, _vp, _i32, _i64, _vp, _vp, _vp, ctypes.c_int, _i64, _i64,
                          _u32, _vp],
+    "fp8_grouped_gemm_swiglu_quant": [_vp, _vp, _vp, _i32, _i64, _vp, _vp, _vp, _vp, _i64, _i64,
+                                      _u32, _vp],
     "fp8_get_device_status": [_vp],
     "fp8fg_status_string": [ctypes.c_int],
     "fp8fg_abi_version": [],
@@ -228,6 +230,34 @@ def grouped_gemm(a, sa, offsets, b, sb, out_dtype=torch.bfloat16, out=None, stre
                                    _ptr(out), _out_code(out.dtype), N, K, 0, _stream(stream)),
            "fp8_grouped_gemm")
     return out
+
+
+def grouped_swiglu_quant(a, sa, offsets, b, sb, pow2: bool = True, out=None, out_scales=None,
+                         stream=None):
+    """Routed up-projection (b [E, 2I, K]: gate rows then up rows) followed by
+    h = silu(g) * u, returned as the down-projection input (q uint8 [T, I],
+    s float32 [T, I/128])."""
+    _need(a, (torch.uint8,), "a")
+    _need(b, (torch.uint8,), "b")
+    _need(sa, (torch.float32,), "sa")
+    _need(sb, (torch.float32,), "sb")
+    _need(offsets, (torch.int32,), "offsets")
+    T, K = a.shape
+    E, N, Kb = b.shape
+    if Kb != K or offsets.numel() != E + 1:
+        raise ValueError("shape mismatch between a, b and offsets")
+    I = N // 2
+    if out is None:
+        out = torch.empty((T, I), dtype=torch.uint8, device=a.device)
+    if out_scales is None:
+        out_scales = torch.empty((T, max(I // 128, 1)), dtype=torch.float32, device=a.device)
+    _need(out, (torch.uint8,), "out")
+    _need(out_scales, (torch.float32,), "out_scales")
+    _check(load().fp8_grouped_gemm_swiglu_quant(_ptr(a), _ptr(sa), _ptr(offsets), E, T, _ptr(b),
+                                                _ptr(sb), _ptr(out), _ptr(out_scales), N, K,
+                                                POW2 if pow2 else 0, _stream(stream)),
+           "fp8_grouped_gemm_swiglu_quant")
+    return out, out_scales
 
 
 def device_status(stream=None) -> int:

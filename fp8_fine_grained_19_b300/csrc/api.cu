@@ -133,7 +133,7 @@ bool have_device() { return device_sm_count() > 0; }
 
 extern "C" {
 
-int fp8fg_abi_version(void) { return 3; }
+int fp8fg_abi_version(void) { return 4; }
 
 const char* fp8fg_status_string(fp8fg_status status) {
   switch (status) {
@@ -258,6 +258,27 @@ fp8fg_status fp8_grouped_gemm(const uint8_t* a, const float* sa, const int32_t* 
   if (!have_device()) return FP8FG_ERR_CUDA;
   return launch_grouped_gemm(a, sa, offsets, E, total_rows, b, sb, c, c_dtype, N, K,
                              as_stream(stream));
+}
+
+fp8fg_status fp8_grouped_gemm_swiglu_quant(const uint8_t* a, const float* sa,
+                                           const int32_t* offsets, int32_t E, int64_t total_rows,
+                                           const uint8_t* b, const float* sb, uint8_t* q, float* s,
+                                           int64_t N, int64_t K, unsigned flags, void* stream) {
+  if ((flags & ~FP8FG_POW2) != 0 || total_rows < 0 || N < 0 || K < 0 || E < 1)
+    return FP8FG_ERR_INVALID_ARG;
+  if (offsets == nullptr || b == nullptr || sb == nullptr ||
+      (total_rows > 0 && (a == nullptr || sa == nullptr || q == nullptr || s == nullptr)))
+    return FP8FG_ERR_INVALID_ARG;
+  if (E > 1024 || K < 128 || K % 128 != 0 || N < 256 || N % 256 != 0 || total_rows > kMaxDim ||
+      N > kMaxDim || K > kMaxDim || static_cast<int64_t>(E) * N > kMaxDim ||
+      (total_rows / 128 + E) * (N / 256) > kMaxDim)
+    return FP8FG_ERR_UNSUPPORTED_SHAPE;
+  if (!aligned16(a) || !aligned16(sa) || !aligned16(b) || !aligned16(sb) || !aligned16(q) ||
+      !aligned16(s) || (reinterpret_cast<uintptr_t>(offsets) & 3u) != 0)
+    return FP8FG_ERR_MISALIGNED;
+  if (!have_device()) return FP8FG_ERR_CUDA;
+  return launch_grouped_swiglu_quant(a, sa, offsets, E, total_rows, b, sb, q, s, N, K,
+                                     (flags & FP8FG_POW2) != 0, as_stream(stream));
 }
 
 fp8fg_status fp8_get_device_status(void* stream) {

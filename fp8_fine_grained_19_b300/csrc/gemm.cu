@@ -63,6 +63,11 @@ constexpr int REGS_LAUNCH = 168;
 constexpr int REGS_PRODUCER = 56;
 constexpr int REGS_EPILOGUE = 224;
 static_assert(2 * REGS_EPILOGUE + REGS_PRODUCER <= 3 * REGS_LAUNCH, "register split");
+// The grouped SwiGLU kernel spills at the 224/56 split (the report does not
+// say where); at 208/88 it compiles without spills.
+constexpr int SWIGLU_REGS_EPILOGUE = 208;
+constexpr int SWIGLU_REGS_PRODUCER = (3 * REGS_LAUNCH - 2 * SWIGLU_REGS_EPILOGUE) / 8 * 8;
+static_assert(2 * SWIGLU_REGS_EPILOGUE + SWIGLU_REGS_PRODUCER <= 3 * REGS_LAUNCH, "register split");
 constexpr int TMEM_COLS = 512;
 constexpr int GROUP_M = 16;
 constexpr int MAX_EXPERTS = 1024;
@@ -70,6 +75,10 @@ constexpr int SB_GROUP = 8;           // tile mode: slices whose B scales are sh
 constexpr int CST_BYTES = 2048;       // output staging per promotion warp: 32 rows x 64 bytes
 constexpr int CST_ROW = 64;           // bytes per staged row (the tensor map's 64-byte swizzle)
 constexpr uint32_t IDESC = idesc_e4m3_f32(BM, BN);
+// Output modes of the kernel's store phase.
+constexpr int EPI_STORE = 0;    // C in BF16 or FP32
+constexpr int EPI_QUANT = 1;    // dense: C as 1x128 E4M3 tiles + scales
+constexpr int EPI_SWIGLU = 2;   // grouped: h = silu(gate) * up as 1x128 E4M3 tiles + scales
 
 struct GemmParams {
   const float* sa;        // [rows, nkb]
@@ -162,7 +171,7 @@ __device__ __forceinline__ Tile tile_of(int t, const GemmParams& p, const Smem& 
   return r;
 }
 
-template <bool GROUPED, bool BTILE, bool OUTQ>
+template <bool GROUPED, bool BTILE, int EPI>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     blockscaled_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                             const __grid_constant__ CUtensorMap tmB,
@@ -248,7 +257,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   const int nkb = p.nkb;
 
   if (warp >= NUM_EPI_WARPS) {
-    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(REGS_PRODUCER));
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(EPI == EPI_SWIGLU ? SWIGLU_REGS_PRODUCER
+                                                                             : REGS_PRODUCER));
     if (warp == PRODUCER_WARP) {
       // ------------------------------------------------------- TMA producer
       if (lane == 0) {
@@ -264,7 +274,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             const uint32_t fb = smem_u32(&sm.full_bar[stage]);
             mbar_arrive_expect_tx(fb, A_BYTES + B_BYTES);
             tma_load_2d(smem_u32(sm.a[stage]), &tmA, fb, kb * BK, tl.m0);
-            if constexpr (GROUPED)
+            if constexpr (EPI == EPI_SWIGLU) {
+              // B rows of the stage: gate j0..j0+63, up j0.., gate j0+64.., up j0+64..
+              // (j0 = n0/2), so each TMEM column half holds g and u of the same
+              // 64 outputs
+              const int j0 = tl.n0 / 2;
+#pragma unroll
+              for (int i = 0; i < 4; ++i)
+                tma_load_3d(smem_u32(sm.b[stage]) + i * (B_BYTES / 4), &tmB, fb, kb * BK,
+                            (i & 1) * (p.N / 2) + j0 + (i >> 1) * 64, tl.e);
+            } else if constexpr (GROUPED)
               tma_load_3d(smem_u32(sm.b[stage]), &tmB, fb, kb * BK, tl.n0, tl.e);
             else
               tma_load_2d(smem_u32(sm.b[stage]), &tmB, fb, kb * BK, tl.n0);
@@ -323,7 +342,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
   } else {
     // ------------------------------------------------ promotion + epilogue
-    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(REGS_EPILOGUE));
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(EPI == EPI_SWIGLU ? SWIGLU_REGS_EPILOGUE
+                                                                             : REGS_EPILOGUE));
     const int quad = warp & 3;                      // TMEM lane quadrant
     const int half = warp >> 2;                     // N half of the tile
     const int tid_h = threadIdx.x & 127;            // index within the half's warpgroup
@@ -341,8 +361,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       // rows and columns past the end read valid scales (row 0 / the last
       // column) and are never stored
       const float* sa_row = p.sa + static_cast<int64_t>(row_ok ? row : 0) * nkb;
+      // B row of this half's first column (SwiGLU: the gate block j0 = n0/2;
+      // the up block is I/128 blocks further, see the K loop)
+      const int brow_h = EPI == EPI_SWIGLU ? tl.n0 / 2 : col_h;
       const float* sb_ptr =
-          p.sb + (static_cast<int64_t>(tl.e) * n_blocks + (half_ok ? col_h / 128 : 0)) * nkb;
+          p.sb + (static_cast<int64_t>(tl.e) * n_blocks + (half_ok ? brow_h / 128 : 0)) * nkb;
 
       uint64_t acc[64];
 #pragma unroll
@@ -414,13 +437,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           break;
         }
       } else {
+        // SwiGLU: columns 64..127 of the half are up rows, whose block scale
+        // lies I/128 blocks after the gate block
+        const float* sbu_ptr = sb_ptr + (EPI == EPI_SWIGLU ? (p.N / 256) * nkb : 0);
         float sa_next = __ldg(sa_row);
         float sb_next = __ldg(sb_ptr);
+        float sbu_next = EPI == EPI_SWIGLU ? __ldg(sbu_ptr) : 0.0f;
         for (int kb = 0; kb < nkb; ++kb, ++it) {
-          const float sa_cur = sa_next, sb_cur = sb_next;
+          const float sa_cur = sa_next, sb_cur = sb_next, sbu_cur = sbu_next;
           if (kb + 1 < nkb) {
             sa_next = __ldg(sa_row + kb + 1);
             sb_next = __ldg(sb_ptr + kb + 1);
+            if constexpr (EPI == EPI_SWIGLU) sbu_next = __ldg(sbu_ptr + kb + 1);
           }
           const uint32_t buf = it & 1, bpar = (it >> 1) & 1;
           if (!mbar_wait(smem_u32(&sm.tfull_bar[buf]), bpar, p.wait_limit, abort_flag, p.status)) {
@@ -431,22 +459,82 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           const uint32_t taddr = lane_taddr + buf * BN;
           const float s = sa_cur * sb_cur;
           const uint64_t s2 = pack2(__float_as_uint(s), __float_as_uint(s));
+          const float su = sa_cur * sbu_cur;
+          const uint64_t su2 = pack2(__float_as_uint(su), __float_as_uint(su));
 #pragma unroll
           for (int c = 0; c < 4; ++c) {
             uint32_t r[32];
             tmem_ld_32cols(taddr + c * 32, r);
             tmem_ld_wait();
+            const uint64_t sc2 = EPI == EPI_SWIGLU && c >= 2 ? su2 : s2;
 #pragma unroll
-            for (int j = 0; j < 16; ++j) fma2(acc[c * 16 + j], pack2(r[2 * j], r[2 * j + 1]), s2);
+            for (int j = 0; j < 16; ++j) fma2(acc[c * 16 + j], pack2(r[2 * j], r[2 * j + 1]), sc2);
           }
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(smem_u32(&sm.tempty_bar[buf]));
         }
-        if (!ok) break;
+        if constexpr (EPI == EPI_SWIGLU) {
+          // the gate/up warp pair meets at the exchange below: both leave
+          // together if either one's K loop gave up
+          if (bar_any(3 + quad, 64, !ok)) {
+            ok = false;
+            break;
+          }
+        } else if (!ok) {
+          break;
+        }
       }
 
-      if constexpr (GROUPED) {
+      if constexpr (EPI == EPI_SWIGLU) {
+        // --- grouped SwiGLU: this thread holds g (accumulator pairs 0..31) and
+        // u (pairs 32..63) of outputs j0 + 64*half .. +63 of its row.  It forms
+        // h = silu(g) * u in FP32 (the exact-silu version measured ~10 % slower
+        // for the whole kernel), the warp pair (same rows, both halves)
+        // combines the 1x128 tile amax through shared memory, and each thread
+        // stores its 64 codes; half 0 stores the tile's scale.  Rows past the
+        // expert's end are not stored.
+        float amax = 0.0f;
+#pragma unroll
+        for (int v = 0; v < 32; ++v) {
+          float g0, g1, u0, u1;
+          unpack2(acc[v], g0, g1);
+          unpack2(acc[32 + v], u0, u1);
+          // silu with the fast exponential and divide: relative error at most
+          // (4 + 1.2 |g|) 2^-23 by their documented bounds (2 + 1.173 |x| ulp and
+          // 2 ulp); below g = -87 the divide returns a zero of the right sign
+          const float h0 = __fmul_rn(__fdividef(g0, __fadd_rn(1.0f, __expf(-g0))), u0);
+          const float h1 = __fmul_rn(__fdividef(g1, __fadd_rn(1.0f, __expf(-g1))), u1);
+          acc[v] = pack2(__float_as_uint(h0), __float_as_uint(h1));
+          amax = fmaxf(amax, fmaxf(fabsf(h0), fabsf(h1)));
+        }
+        // amax slots: [half][quad][lane]; the partner's slot is rewritten only
+        // after the next tile's pair vote, which follows this read
+        float* am = reinterpret_cast<float*>(sm.cst[0]);
+        am[(half * 4 + quad) * 32 + lane] = amax;
+        bar_sync(3 + quad, 64);
+        amax = fmaxf(amax, am[((half ^ 1) * 4 + quad) * 32 + lane]);
+        if (row_ok) {
+          const Scale sc = scale_from_amax(amax, p.pow2_out != 0);
+          const int I = p.N / 2;
+          const int j0 = tl.n0 / 2;
+          if (half == 0) p.s_out[static_cast<int64_t>(row) * (I / 128) + j0 / 128] = sc.s;
+          uint8_t* dst = static_cast<uint8_t*>(p.c) + static_cast<int64_t>(row) * I + j0 + 64 * half;
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {           // 16 codes = outputs 16i .. 16i+15
+            uint32_t w[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              float x0, x1, x2, x3;
+              unpack2(acc[8 * i + 2 * k], x0, x1);
+              unpack2(acc[8 * i + 2 * k + 1], x2, x3);
+              w[k] = e4m3x2(__fmul_rn(x0, sc.m), __fmul_rn(x1, sc.m)) |
+                     (e4m3x2(__fmul_rn(x2, sc.m), __fmul_rn(x3, sc.m)) << 16);
+            }
+            *reinterpret_cast<uint4*>(dst + 16 * i) = make_uint4(w[0], w[1], w[2], w[3]);
+          }
+        }
+      } else if constexpr (GROUPED) {
         // --- grouped: each thread stores its row segment (128 columns of its
         // half); rows past the expert's end belong to the next expert
         if (row_ok && half_ok) {
@@ -476,7 +564,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             }
           }
         }
-      } else if constexpr (OUTQ) {
+      } else if constexpr (EPI == EPI_QUANT) {
         // --- dense, E4M3 output: the thread's 128 columns of its row are one
         // 1x128 tile; the same amax/scale/multiplier rules as act_quant apply
         // to the FP32 accumulator, and the codes leave like the BF16 output
@@ -619,7 +707,7 @@ __global__ void wait_timeout_selftest_kernel(long long limit, int* status) {
 constexpr size_t kSmemBytes = sizeof(Smem) + 1024;
 
 bool make_maps(CUtensorMap* mA, CUtensorMap* mB, const uint8_t* a, int64_t rowsA,
-               const uint8_t* b, int64_t E, int64_t N, int64_t K) {
+               const uint8_t* b, int64_t E, int64_t N, int64_t K, uint32_t b_box_rows = BN) {
   const uint64_t dA[2] = {static_cast<uint64_t>(K), static_cast<uint64_t>(rowsA)};
   const uint64_t sA[1] = {static_cast<uint64_t>(K)};
   const uint32_t boxA[2] = {BK, BM};
@@ -633,7 +721,7 @@ bool make_maps(CUtensorMap* mA, CUtensorMap* mB, const uint8_t* a, int64_t rowsA
   const uint64_t dB[3] = {static_cast<uint64_t>(K), static_cast<uint64_t>(N),
                           static_cast<uint64_t>(E)};
   const uint64_t sB[2] = {static_cast<uint64_t>(K), static_cast<uint64_t>(N * K)};
-  const uint32_t boxB[3] = {BK, BN, 1};
+  const uint32_t boxB[3] = {BK, b_box_rows, 1};
   return encode_tensor_map_u8(mB, b, 3, dB, sB, boxB);
 }
 
@@ -649,10 +737,10 @@ bool make_c_map(CUtensorMap* mC, void* c, fp8fg_dtype ct, int64_t rows, int64_t 
                            c, 2, dC, sC, boxC, CU_TENSOR_MAP_SWIZZLE_64B);
 }
 
-template <bool GROUPED, bool BTILE, bool OUTQ = false>
+template <bool GROUPED, bool BTILE, int EPI = EPI_STORE>
 cudaError_t set_smem_attr() {
   static const cudaError_t e = cudaFuncSetAttribute(
-      blockscaled_gemm_kernel<GROUPED, BTILE, OUTQ>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+      blockscaled_gemm_kernel<GROUPED, BTILE, EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
       static_cast<int>(kSmemBytes));
   return e;
 }
@@ -686,9 +774,9 @@ fp8fg_status launch_gemm(const uint8_t* a, const float* sa, const uint8_t* b, co
   const int tiles = p.m_tiles * p.n_tiles;
   const int grid = tiles < device_sm_count() ? tiles : device_sm_count();
   if (b_tile)
-    blockscaled_gemm_kernel<false, true, false><<<grid, NUM_THREADS, kSmemBytes, st>>>(mA, mB, mC, p);
+    blockscaled_gemm_kernel<false, true, EPI_STORE><<<grid, NUM_THREADS, kSmemBytes, st>>>(mA, mB, mC, p);
   else
-    blockscaled_gemm_kernel<false, false, false><<<grid, NUM_THREADS, kSmemBytes, st>>>(mA, mB, mC, p);
+    blockscaled_gemm_kernel<false, false, EPI_STORE><<<grid, NUM_THREADS, kSmemBytes, st>>>(mA, mB, mC, p);
   return cudaGetLastError() == cudaSuccess ? FP8FG_OK : FP8FG_ERR_CUDA;
 }
 
@@ -704,7 +792,7 @@ fp8fg_status launch_gemm_quant(const uint8_t* a, const float* sa, const uint8_t*
   if (!encode_tensor_map(&mQ, CU_TENSOR_MAP_DATA_TYPE_UINT8, q, 2, dQ, sQ, boxQ,
                          CU_TENSOR_MAP_SWIZZLE_64B))
     return FP8FG_ERR_CUDA;
-  if ((b_tile ? set_smem_attr<false, true, true>() : set_smem_attr<false, false, true>()) !=
+  if ((b_tile ? set_smem_attr<false, true, EPI_QUANT>() : set_smem_attr<false, false, EPI_QUANT>()) !=
       cudaSuccess)
     return FP8FG_ERR_CUDA;
   GemmParams p{};
@@ -728,9 +816,9 @@ fp8fg_status launch_gemm_quant(const uint8_t* a, const float* sa, const uint8_t*
   const int tiles = p.m_tiles * p.n_tiles;
   const int grid = tiles < device_sm_count() ? tiles : device_sm_count();
   if (b_tile)
-    blockscaled_gemm_kernel<false, true, true><<<grid, NUM_THREADS, kSmemBytes, st>>>(mA, mB, mQ, p);
+    blockscaled_gemm_kernel<false, true, EPI_QUANT><<<grid, NUM_THREADS, kSmemBytes, st>>>(mA, mB, mQ, p);
   else
-    blockscaled_gemm_kernel<false, false, true><<<grid, NUM_THREADS, kSmemBytes, st>>>(mA, mB, mQ, p);
+    blockscaled_gemm_kernel<false, false, EPI_QUANT><<<grid, NUM_THREADS, kSmemBytes, st>>>(mA, mB, mQ, p);
   return cudaGetLastError() == cudaSuccess ? FP8FG_OK : FP8FG_ERR_CUDA;
 }
 
@@ -759,8 +847,41 @@ fp8fg_status launch_grouped_gemm(const uint8_t* a, const float* sa, const int32_
   p.b_tile = 0;
   p.wait_limit = wait_limit_cycles();
   p.status = device_status_word();
-  blockscaled_gemm_kernel<true, false, false><<<device_sm_count(), NUM_THREADS, kSmemBytes, st>>>(
+  blockscaled_gemm_kernel<true, false, EPI_STORE><<<device_sm_count(), NUM_THREADS, kSmemBytes, st>>>(
       mA, mB, mC, p);
+  return cudaGetLastError() == cudaSuccess ? FP8FG_OK : FP8FG_ERR_CUDA;
+}
+
+fp8fg_status launch_grouped_swiglu_quant(const uint8_t* a, const float* sa,
+                                         const int32_t* offsets, int32_t E, int64_t total_rows,
+                                         const uint8_t* b, const float* sb, uint8_t* q, float* s,
+                                         int64_t N, int64_t K, bool pow2, cudaStream_t st) {
+  CUtensorMap mA, mB;
+  // B is read as four 64-row boxes per stage (gate, up, gate, up)
+  if (!make_maps(&mA, &mB, a, total_rows > 0 ? total_rows : 1, b, E, N, K, BN / 4))
+    return FP8FG_ERR_CUDA;
+  if (set_smem_attr<true, false, EPI_SWIGLU>() != cudaSuccess) return FP8FG_ERR_CUDA;
+  GemmParams p{};
+  p.sa = sa;
+  p.sb = sb;
+  p.c = q;
+  p.offsets = offsets;
+  p.M = static_cast<int>(total_rows);
+  p.N = static_cast<int>(N);
+  p.K = static_cast<int>(K);
+  p.nkb = static_cast<int>(K / BK);
+  p.m_tiles = 0;
+  p.n_tiles = static_cast<int>(N / BN);       // one tile: 128 outputs = 128 gate + 128 up rows
+  p.E = E;
+  p.c_f32 = 0;
+  p.b_tile = 0;
+  p.s_out = s;
+  p.pow2_out = pow2 ? 1 : 0;
+  p.wait_limit = wait_limit_cycles();
+  p.status = device_status_word();
+  // the C map is not used in this mode; any valid map fills the parameter
+  blockscaled_gemm_kernel<true, false, EPI_SWIGLU><<<device_sm_count(), NUM_THREADS, kSmemBytes,
+                                                     st>>>(mA, mB, mA, p);
   return cudaGetLastError() == cudaSuccess ? FP8FG_OK : FP8FG_ERR_CUDA;
 }
 

@@ -37,6 +37,11 @@ fp8fg_status launch_gemm_quant(const uint8_t* a, const float* sa, const uint8_t*
 fp8fg_status launch_grouped_gemm(const uint8_t* a, const float* sa, const int32_t* offsets,
                                  int32_t E, int64_t total_rows, const uint8_t* b, const float* sb,
                                  void* c, fp8fg_dtype ct, int64_t N, int64_t K, cudaStream_t st);
+// Grouped up-projection with SwiGLU; h leaves as 1x128 E4M3 tiles (q, s).
+fp8fg_status launch_grouped_swiglu_quant(const uint8_t* a, const float* sa,
+                                         const int32_t* offsets, int32_t E, int64_t total_rows,
+                                         const uint8_t* b, const float* sb, uint8_t* q, float* s,
+                                         int64_t N, int64_t K, bool pow2, cudaStream_t st);
 // Failure-detection self-test: one wait that nothing completes.
 cudaError_t launch_wait_timeout_selftest(uint32_t limit_cycles, cudaStream_t st);
 

@@ -173,6 +173,32 @@ fp8fg_status fp8_grouped_gemm(const uint8_t* a, const float* sa, const int32_t* 
                               void* stream);
 
 /*
+ * fp8_grouped_gemm_swiglu_quant -- the routed up-projection followed by SwiGLU,
+ * leaving h as the down-projection's FP8 input.  Source: page 2, passage
+ * quantising the MoE up-projection input for FP8 Fprop and the power-of-2
+ * passage naming the activations cached with integral power-of-2 scales; page
+ * 5, MoE configuration passage (expert hidden size 2048).  Readings (the pages
+ * name neither): the activation is SwiGLU, h = silu(g) * u, and each expert's
+ * up-projection rows are its I gate rows followed by its I up rows.
+ *
+ * a, sa, offsets, E, total_rows as fp8_grouped_gemm (offsets checked on the
+ * device, FP8FG_ERR_BAD_OFFSETS, nothing written).
+ * b  [E, N, K] codes with N = 2I (gate rows 0..I-1, up rows I..2I-1);
+ *    sb [E, N/128, K/128] FP32 (128x128 blocks).
+ * q  [total_rows, I] E4M3 codes of h; s [total_rows, I/128] FP32 scales.
+ * g and u are the FP32 accumulators of the promoted sums; h = g / (1 + e^-g) * u
+ * in FP32 with the fast exponential and divide (relative error of silu at most
+ * (4 + 1.2 |g|) 2^-23, a zero of the right sign below g = -87); per 1x128 tile of h the
+ * activation quantiser's rules apply, power-of-2 scales with FP8FG_POW2 (the
+ * pages' choice for this tensor).
+ * Requires 1 <= E <= 1024, N % 256 == 0, K % 128 == 0; flags within FP8FG_POW2.
+ */
+fp8fg_status fp8_grouped_gemm_swiglu_quant(const uint8_t* a, const float* sa,
+                                           const int32_t* offsets, int32_t E, int64_t total_rows,
+                                           const uint8_t* b, const float* sb, uint8_t* q, float* s,
+                                           int64_t N, int64_t K, unsigned flags, void* stream);
+
+/*
  * fp8_get_device_status -- synchronises `stream`, then returns and clears the
  * library status word (FP8FG_OK, FP8FG_ERR_TIMEOUT or FP8FG_ERR_BAD_OFFSETS);
  * FP8FG_ERR_CUDA if the synchronisation itself failed.

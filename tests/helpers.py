@@ -83,3 +83,56 @@ def oracle_gemm_chunked(qa, sa, qb, sb, b_tile=False, chunk=2048) -> np.ndarray:
         sbc = sb[c0:c1] if b_tile else sb[c0 // 128:(c1 + 127) // 128]
         parts.append(oracle.gemm(qa, sa, qb[c0:c1], sbc, b_tile=b_tile))
     return np.concatenate(parts, axis=1)
+
+
+_E4M3_MAGS = None
+
+
+def check_quant_decisions(q_gpu, s_gpu, x_ref, err, pow2):
+    """Compare GPU 1x128-tile quantisation of values the GPU computed with rounding
+    error against the oracle's quantisation of the exact values.
+
+    x_ref: oracle float32 values [M, N]; err: per-element bound on |x_gpu - x_ref|
+    (float64 [M, N]).  Scales must agree within the amax's share of err
+    (exactly for power-of-2 scales unless amax/448 lies that close to a power of
+    two); codes must equal the oracle's unless x * m lies within the error of an
+    E4M3 rounding midpoint, where either neighbour is correct; every code must
+    decode to within one E4M3 step of x.  Returns the fraction of codes decided.
+    """
+    import oracle
+    from oracle import e4m3
+
+    global _E4M3_MAGS
+    if _E4M3_MAGS is None:
+        _E4M3_MAGS = np.unique(np.abs(e4m3.decode(np.arange(0x7F, dtype=np.uint8))))
+    mags = _E4M3_MAGS
+    q_o, s_o = oracle.act_quant(x_ref, pow2)
+    M, N = q_o.shape
+    xt = x_ref.astype(np.float64).reshape(M, N // 128, 128)
+    Et = np.asarray(err, dtype=np.float64).reshape(M, N // 128, 128)
+    so = s_o.astype(np.float64)
+    sg = np.asarray(s_gpu, dtype=np.float64)
+    amax = np.abs(xt).max(axis=2)
+    e_amax = Et.max(axis=2)
+    if not pow2:
+        tol = amax / 448.0 * 2.0 ** -22 + e_amax / 448.0 * 1.01
+        assert np.all(np.abs(sg - so) <= tol), "scale outside the error bound"
+    else:
+        lo2 = np.log2(np.maximum((amax - e_amax) / 448.0, 2.0 ** -80))
+        hi2 = np.log2((amax + e_amax) / 448.0 * (1 + 2.0 ** -22))
+        ambiguous = np.ceil(lo2) != np.ceil(hi2)
+        assert np.all((sg == so) | ambiguous), "power-of-2 scale differs away from a power of 2"
+    m = 1.0 / so[:, :, None]
+    y = np.abs(xt) * m
+    idx = np.clip(np.searchsorted(mags, y), 1, len(mags) - 1)
+    mid_hi = (mags[idx - 1] + mags[idx]) / 2
+    mid_lo = (mags[np.clip(idx - 2, 0, None)] + mags[idx - 1]) / 2
+    near = np.minimum(np.abs(y - mid_hi), np.abs(y - mid_lo))
+    slack = Et * m * 1.01 + y * 2.0 ** -21 + np.abs(sg[:, :, None] / so[:, :, None] - 1) * y
+    sure = (near > slack).reshape(M, N)
+    qg = np.asarray(q_gpu).reshape(M, N)
+    assert np.array_equal(qg[sure], q_o[sure]), "code differs where the rounding is decided"
+    dq = e4m3.decode(qg).astype(np.float64).reshape(M, N // 128, 128) * sg[:, :, None]
+    step = (np.maximum(y, 2.0 ** -6) * 2.0 ** -3 + 2.0 ** -9) * so[:, :, None]
+    assert np.all(np.abs(dq - xt) <= step + Et), "code off by more than one step"
+    return float(sure.mean())

@@ -29,7 +29,6 @@ from tests import helpers as H
 pytestmark = pytest.mark.gpu
 
 FINITE = np.array([c for c in range(256) if (c & 0x7F) != 0x7F], dtype=np.uint8)
-E4M3_MAGS = np.unique(np.abs(e4m3.decode(np.arange(0x7F, dtype=np.uint8))))   # 0 .. 448
 
 
 def _operands(M, N, K, seed, b_tile):
@@ -54,41 +53,10 @@ def _abs_sum(qa, sa, qb, sb, b_tile):
 def _check_against_oracle(q_gpu, s_gpu, qa, sa, qb, sb, b_tile, pow2, rows=None):
     if rows is not None:
         qa, sa = qa[rows], sa[rows]
-    q_o, s_o, x_o = oracle.gemm_quant(qa, sa, qb, sb, b_tile=b_tile, pow2=pow2)
+    _, _, x_o = oracle.gemm_quant(qa, sa, qb, sb, b_tile=b_tile, pow2=pow2)
     nkb = qa.shape[1] // 128
-    E = (nkb + 1) * 2.0 ** -24 * _abs_sum(qa, sa, qb, sb, b_tile)       # bound on |C32 - C|
-    M, N = q_o.shape
-    xt = x_o.astype(np.float64).reshape(M, N // 128, 128)
-    Et = E.reshape(M, N // 128, 128)
-    so = s_o.astype(np.float64)[:, :, None]
-    sg = s_gpu.astype(np.float64)
-    amax = np.abs(xt).max(axis=2)
-    e_amax = Et.max(axis=2)
-    # scales
-    if not pow2:
-        tol = amax / 448.0 * 2.0 ** -22 + e_amax / 448.0 * 1.01
-        assert np.all(np.abs(sg - s_o) <= tol), "scale outside the FP32-sum bound"
-    else:
-        lo2 = np.log2(np.maximum((amax - e_amax) / 448.0, 2.0 ** -80))
-        hi2 = np.log2((amax + e_amax) / 448.0 * (1 + 2.0 ** -22))
-        ambiguous = np.ceil(lo2) != np.ceil(hi2)
-        assert np.all((sg == s_o) | ambiguous), "power-of-2 scale differs away from a power of 2"
-    # codes: the oracle's y = x / s and its distance to the nearest rounding midpoint
-    m = 1.0 / so
-    y = np.abs(xt) * m
-    idx = np.clip(np.searchsorted(E4M3_MAGS, y), 1, len(E4M3_MAGS) - 1)
-    mids = (E4M3_MAGS[idx - 1] + E4M3_MAGS[idx]) / 2
-    near = np.minimum(np.abs(y - mids),
-                      np.abs(y - (E4M3_MAGS[np.clip(idx - 2, 0, None)] + E4M3_MAGS[idx - 1]) / 2))
-    slack = Et * m * 1.01 + y * 2.0 ** -21 + np.abs(sg[:, :, None] / so - 1) * y
-    sure = (near > slack).reshape(M, N)
-    qg = q_gpu.reshape(M, N)
-    assert np.array_equal(qg[sure], q_o[sure]), "code differs where the rounding is decided"
-    # elsewhere: the GPU code decodes (with its own scale) to within one E4M3 step of x
-    dq = e4m3.decode(qg).astype(np.float64).reshape(M, N // 128, 128) * sg[:, :, None]
-    step = np.maximum(y, 2.0 ** -6) * 2.0 ** -3 * so + 2.0 ** -9 * so
-    assert np.all(np.abs(dq - xt) <= step + Et), "code off by more than one step"
-    return float(sure.mean())
+    err = (nkb + 1) * 2.0 ** -24 * _abs_sum(qa, sa, qb, sb, b_tile)     # bound on |C32 - C|
+    return H.check_quant_decisions(q_gpu, s_gpu, x_o, err, pow2)
 
 
 @pytest.mark.parametrize("pow2", [False, True])

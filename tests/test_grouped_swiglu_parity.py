@@ -1,0 +1,187 @@
+"""GPU routed up-projection + SwiGLU quantised for the down-projection, vs the oracle.
+
+oracle.grouped_swiglu_quant: per expert, g and u are the gate and up halves of
+the promoted up-projection; h = silu(g) * u is quantised into 1x128 tiles with
+power-of-2 scales (page 2, inprokorea.com free #735329, power-of-2 passage).
+
+The GPU forms g and u as FP32 sums (each off by at most
+E = (nkb + 1) * 2^-24 * sum_kb |P_kb sa sb|) and h = g / (1 + expf(-g)) * u in
+FP32 with the fast exponential and divide, whose documented bounds (2 + 1.173|x|
+ulp and 2 ulp) give silu a relative error of at most (4 + 1.2|g|) 2^-23; below
+g = -87 the divide returns zero, counted here as an error of |h|.  With
+|silu'| <= 1.1:  |h_gpu - h| <= |silu(g)| Eu + 1.1 |u| Eg + Eg Eu
++ ((4 + 1.2|g|) 2^-23 + 2^-24) |h|.  Codes must equal the oracle's wherever that
+bound cannot move h / s across an E4M3 rounding midpoint.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from oracle import e4m3
+from tests import helpers as H
+
+pytestmark = pytest.mark.gpu
+
+FINITE = np.array([c for c in range(256) if (c & 0x7F) != 0x7F], dtype=np.uint8)
+
+
+def _abs_grouped(qa, sa, off, qb, sb):
+    """sum_kb |P_kb| sa sb per element of the grouped product (float64 [T, N])."""
+    T, N = qa.shape[0], qb.shape[1]
+    out = np.zeros((T, N))
+    for e in range(len(off) - 1):
+        r0, r1 = int(off[e]), int(off[e + 1])
+        if r1 == r0:
+            continue
+        P = np.abs(oracle.slice_partials(qa[r0:r1], qb[e]))
+        for kb in range(P.shape[0]):
+            out[r0:r1] += (P[kb] * sa[r0:r1, kb].astype(np.float64)[:, None]
+                           * np.repeat(sb[e][:, kb].astype(np.float64), 128)[None, :])
+    return out
+
+
+def _h_error_bound(qa, sa, off, qb, sb):
+    nkb = qa.shape[1] // 128
+    I = qb.shape[1] // 2
+    C = oracle.grouped_gemm(qa, sa, off, qb, sb)
+    E = (nkb + 1) * 2.0 ** -24 * _abs_grouped(qa, sa, off, qb, sb)
+    g, u, Eg, Eu = C[:, :I], C[:, I:], E[:, :I], E[:, I:]
+    h = oracle.silu(g) * u
+    rel = (4 + 1.2 * np.abs(g)) * 2.0 ** -23 + 2.0 ** -24
+    err = np.abs(oracle.silu(g)) * Eu + 1.1 * np.abs(u) * Eg + Eg * Eu + rel * np.abs(h)
+    return np.where(g < -87.0, err + np.abs(h), err)
+
+
+def _random_case(sizes, I, K, seed):
+    g = np.random.default_rng(seed)
+    T, E = int(sum(sizes)), len(sizes)
+    qa = e4m3.encode((g.standard_normal((T, K)) * 30).astype(np.float32))
+    qb = e4m3.encode((g.standard_normal((E, 2 * I, K)) * 30).astype(np.float32))
+    sa = np.exp2(g.integers(-9, -5, (T, K // 128))).astype(np.float32)
+    sb = np.exp(g.uniform(-6, -3, (E, 2 * I // 128, K // 128))).astype(np.float32)
+    off = np.concatenate([[0], np.cumsum(sizes)]).astype(np.int32)
+    return qa, sa, off, qb, sb
+
+
+@pytest.mark.parametrize("sizes,I,K", [([5, 0, 300, 129, 1], 256, 512), ([128], 128, 128),
+                                       ([0, 0, 260, 0], 384, 256)])
+def test_swiglu_quant_vs_oracle(cuda_lib, sizes, I, K):
+    qa, sa, off, qb, sb = _random_case(sizes, I, K, sum(sizes) + I + K)
+    T = qa.shape[0]
+    raw_q, q = H.guarded_empty((T, I), torch.uint8)
+    raw_s, s = H.guarded_empty((T, I // 128), torch.float32)
+    cuda_lib.grouped_swiglu_quant(*[H.to_dev(v) for v in (qa, sa, off, qb, sb)], out=q, out_scales=s)
+    torch.cuda.synchronize()
+    assert cuda_lib.device_status() == 0
+    assert H.guards_intact(raw_q) and H.guards_intact(raw_s), "write outside the outputs"
+    _, _, h_o = oracle.grouped_swiglu_quant(qa, sa, off, qb, sb, pow2=True)
+    decided = H.check_quant_decisions(q.cpu().numpy(), s.cpu().numpy(), h_o,
+                                      _h_error_bound(qa, sa, off, qb, sb), pow2=True)
+    assert decided > 0.99
+
+
+def test_swiglu_quant_exact_case(cuda_lib):
+    # gate = 64 exactly (silu(64) = 64 in FP32 too), up = E4M3 values with a 448
+    # per tile: h = 64 * up, scale 64, the up codes come back
+    g = np.random.default_rng(31)
+    sizes, I, K = [3, 0, 130], 256, 128
+    T, E = sum(sizes), len(sizes)
+    qa = np.zeros((T, K), np.uint8)
+    qa[:, 0] = 0x38
+    qb = np.zeros((E, 2 * I, K), np.uint8)
+    ups = []
+    for e in range(E):
+        codes = g.choice(FINITE, size=I).astype(np.uint8)
+        codes[[7, 200]] = 0x7E
+        qb[e, :I, 0] = 0x68
+        qb[e, I:, 0] = codes
+        ups.append(np.where(codes == 0x80, 0, codes).astype(np.uint8))
+    off = np.concatenate([[0], np.cumsum(sizes)]).astype(np.int32)
+    sa = np.ones((T, 1), np.float32)
+    sb = np.ones((E, 2 * I // 128, 1), np.float32)
+    q, s = cuda_lib.grouped_swiglu_quant(*[H.to_dev(v) for v in (qa, sa, off, qb, sb)])
+    q_o, s_o, _ = oracle.grouped_swiglu_quant(qa, sa, off, qb, sb)
+    assert np.array_equal(q.cpu().numpy(), q_o) and np.array_equal(s.cpu().numpy(), s_o)
+    assert np.all(s_o == 64.0)
+    assert np.array_equal(q_o[0], ups[0]) and np.array_equal(q_o[-1], ups[2])
+
+
+def test_swiglu_rejects_bad_offsets_on_device(cuda_lib):
+    qa, sa, off, qb, sb = _random_case([130, 2], 128, 128, 3)
+    bad = off.copy()
+    bad[1] = bad[2] + 1                                   # decreasing
+    q = torch.full((qa.shape[0], 128), 0x5A, dtype=torch.uint8, device="cuda")
+    s = torch.zeros((qa.shape[0], 1), dtype=torch.float32, device="cuda")
+    cuda_lib.grouped_swiglu_quant(*[H.to_dev(v) for v in (qa, sa, bad, qb, sb)], out=q, out_scales=s)
+    assert cuda_lib.device_status() == cuda_lib.ERR_BAD_OFFSETS
+    assert bool((q == 0x5A).all()) and bool((s == 0).all())
+
+
+def test_small_routed_layer_fused_end_to_end(cuda_lib):
+    """tokens -> act_quant (pow2) -> gather -> fused up + SwiGLU -> down, vs the oracle chain."""
+    case = synth.MOE_SMALL
+    tok = case.tokens()
+    r = synth.moe_route(H.f32(tok), case.router(), case.bias(), case.topk)
+    off = r["offsets"]
+    qx, sx = cuda_lib.act_quant(tok.cuda(), pow2=True)
+    qx_r, sx_r = oracle.act_quant(H.f32(tok), pow2=True)
+    assert np.array_equal(qx.cpu().numpy(), qx_r)
+    idx = torch.from_numpy(r["token_of_row"]).cuda()
+    qa, sa = qx.index_select(0, idx).contiguous(), sx.index_select(0, idx).contiguous()
+    qa_r, sa_r = qx_r[r["token_of_row"]], sx_r[r["token_of_row"]]
+    wu = torch.stack([synth.expert_weight(case, e, "up") for e in range(case.E)])
+    wd = torch.stack([synth.expert_weight(case, e, "down") for e in range(case.E)])
+    qu, su = cuda_lib.weight_quant(wu.reshape(-1, case.H).cuda())
+    qd, sd = cuda_lib.weight_quant(wd.reshape(-1, case.I).cuda())
+    qu_r, su_r = oracle.weight_quant(H.f32(wu.reshape(-1, case.H)))
+    qd_r, sd_r = oracle.weight_quant(H.f32(wd.reshape(-1, case.I)))
+    qu_r = qu_r.reshape(case.E, 2 * case.I, case.H)
+    su_r = su_r.reshape(case.E, 2 * case.I // 128, case.H // 128)
+    dev_off = H.to_dev(off.astype(np.int32))
+    qh, sh = cuda_lib.grouped_swiglu_quant(qa, sa, dev_off, qu.view(case.E, 2 * case.I, case.H),
+                                           su.view(case.E, 2 * case.I // 128, case.H // 128))
+    qh_r, sh_r, h_r = oracle.grouped_swiglu_quant(qa_r, sa_r, off, qu_r, su_r, pow2=True)
+    decided = H.check_quant_decisions(qh.cpu().numpy(), sh.cpu().numpy(), h_r,
+                                      _h_error_bound(qa_r, sa_r, off, qu_r, su_r), pow2=True)
+    assert decided > 0.99
+    down = cuda_lib.grouped_gemm(qh, sh, dev_off, qd.view(case.E, case.H, case.I),
+                                 sd.view(case.E, case.H // 128, case.I // 128), out_dtype=torch.float32)
+    ref = oracle.grouped_gemm(qh_r, sh_r, off, qd_r.reshape(case.E, case.H, case.I),
+                              sd_r.reshape(case.E, case.H // 128, case.I // 128))
+    # the only differences are the few undecided h codes (one E4M3 step each)
+    assert H.normwise_rel_err(down, ref) <= 1e-3
+
+
+def test_swiglu_quant_extreme_gates(cuda_lib):
+    # gates from {-448, -96, -1, 0, 1, 96, 448}: silu(-448) underflows to a
+    # signed zero on both sides, silu(448) = 448; up values are E4M3 values
+    g = np.random.default_rng(41)
+    sizes, I, K = [130, 3], 256, 128
+    T, E = sum(sizes), len(sizes)
+    gate_codes = np.array([0xFE, 0xEC, 0xB8, 0x00, 0x38, 0x6C, 0x7E], np.uint8)
+    qa = np.zeros((T, K), np.uint8)
+    qa[:, 0] = 0x38
+    qb = np.zeros((E, 2 * I, K), np.uint8)
+    qb[:, :I, 0] = g.choice(gate_codes, size=(E, I))
+    qb[:, I:, 0] = g.choice(FINITE, size=(E, I))
+    off = np.concatenate([[0], np.cumsum(sizes)]).astype(np.int32)
+    sa = np.ones((T, 1), np.float32)
+    sb = np.ones((E, 2 * I // 128, 1), np.float32)
+    q, s = cuda_lib.grouped_swiglu_quant(*[H.to_dev(v) for v in (qa, sa, off, qb, sb)])
+    _, _, h_o = oracle.grouped_swiglu_quant(qa, sa, off, qb, sb, pow2=True)
+    H.check_quant_decisions(q.cpu().numpy(), s.cpu().numpy(), h_o,
+                            _h_error_bound(qa, sa, off, qb, sb), pow2=True)
+    # silu is exact on both sides for gates 0 and +-448 (448, a signed zero):
+    # those codes must equal the oracle's wherever the tile scales agree
+    q_o, s_o, _ = oracle.grouped_swiglu_quant(qa, sa, off, qb, sb, pow2=True)
+    gates = np.zeros((T, I), np.uint8)
+    for e in range(E):
+        gates[off[e]:off[e + 1]] = qb[e, :I, 0]
+    exact = np.isin(gates, [0x00, 0x7E, 0xFE])
+    same = np.repeat(s.cpu().numpy() == s_o, 128, axis=1)
+    sel = exact & same
+    assert sel.sum() > T * I // 4
+    assert np.array_equal(q.cpu().numpy()[sel], q_o[sel])

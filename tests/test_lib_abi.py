@@ -40,7 +40,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_abi_version_and_status_strings(lib):
-    assert lib.fp8fg_abi_version() == 3
+    assert lib.fp8fg_abi_version() == 4
     for code in range(7):
         assert fp8.status_string(code)
     assert "unknown" in fp8.status_string(99)
@@ -121,6 +121,21 @@ def test_grouped_rejections(lib):
     assert f(*args(E=2000)) == fp8.ERR_UNSUPPORTED_SHAPE
     assert f(*args(N=200)) == fp8.ERR_UNSUPPORTED_SHAPE
     assert f(*args(off=A16 + 2)) == fp8.ERR_MISALIGNED
+
+
+def test_grouped_swiglu_rejections(lib):
+    f = lib.fp8_grouped_gemm_swiglu_quant
+    args = lambda E=4, T=512, N=512, K=256, flags=fp8.POW2, off=A16, s=A16: (
+        A16, A16, off, E, T, A16, A16, A16, s, N, K, flags, None)
+    assert f(*args(E=0)) == fp8.ERR_INVALID_ARG
+    assert f(*args(off=None)) == fp8.ERR_INVALID_ARG
+    assert f(*args(s=None)) == fp8.ERR_INVALID_ARG
+    assert f(*args(flags=fp8.TRANSPOSE)) == fp8.ERR_INVALID_ARG
+    assert f(*args(N=384)) == fp8.ERR_UNSUPPORTED_SHAPE                  # 2I % 256
+    assert f(*args(K=200)) == fp8.ERR_UNSUPPORTED_SHAPE
+    assert f(*args(E=2000)) == fp8.ERR_UNSUPPORTED_SHAPE
+    assert f(*args(off=A16 + 2)) == fp8.ERR_MISALIGNED
+    assert f(*args(s=MIS)) == fp8.ERR_MISALIGNED
 
 
 def test_selftest_rejects_bad_limit(lib):
