@@ -30,6 +30,10 @@ Pins (checked in tests/test_oracle_*.py without a GPU):
          h = 64 * up and the up codes come back under scale 64; swapping the
          gate and up halves changes the result; power-of-2 scales and the
          half-step bound on random tiles.
+  accum  (accumulation.py, a model of limited-width aligned accumulation)
+         full width is an exact sum; terms below the last kept bit vanish and
+         terms at it are kept; group sums are exact before alignment; error of
+         at most one truncation step per group; fewer bits, larger error.
 Parity unpinned: the "about 2% error at K=4096 with ~14-bit accumulation"
 figure (no mechanism detail to reproduce it); it is context only.
 """
