@@ -20,13 +20,13 @@ __all__ = [
     "gemm_quant", "grouped_gemm", "grouped_swiglu_quant",
     "device_status", "set_wait_limit", "selftest_wait_timeout", "status_string",
     "OK", "ERR_INVALID_ARG", "ERR_UNSUPPORTED_SHAPE", "ERR_MISALIGNED", "ERR_CUDA",
-    "ERR_TIMEOUT", "ERR_BAD_OFFSETS", "POW2", "TRANSPOSE", "B_TILE1x128", "BF16", "F32",
+    "ERR_TIMEOUT", "ERR_BAD_OFFSETS", "POW2", "TRANSPOSE", "B_TILE1x128", "WHOLE_K", "BF16", "F32",
 ]
 
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED_SHAPE, ERR_MISALIGNED, ERR_CUDA, ERR_TIMEOUT, \
     ERR_BAD_OFFSETS = range(7)
 BF16, F32 = 0, 1
-POW2, TRANSPOSE, B_TILE1x128 = 1, 2, 4
+POW2, TRANSPOSE, B_TILE1x128, WHOLE_K = 1, 2, 4, 8
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _LIB: ctypes.CDLL | None = None
@@ -168,8 +168,12 @@ def _out_code(dtype) -> int:
     raise ValueError(f"unsupported output dtype {dtype}")
 
 
-def gemm(a, sa, b, sb, out_dtype=torch.bfloat16, b_tile: bool = False, out=None, stream=None):
-    """C[M, N] = sum_kb (A_kb . B_kb^T) * sa[:, kb] * sb(., kb), promoted to FP32 per 128 K."""
+def gemm(a, sa, b, sb, out_dtype=torch.bfloat16, b_tile: bool = False, out=None, stream=None,
+         whole_k: bool = False):
+    """C[M, N] = sum_kb (A_kb . B_kb^T) * sa[:, kb] * sb(., kb), promoted to FP32 per 128 K.
+
+    whole_k: study mode without promotion (all of K in the tensor core, scaled by
+    sa[0, 0] * sb[0, 0])."""
     for t, n in ((a, "a"), (b, "b")):
         _need(t, (torch.uint8,), n)
     for t, n in ((sa, "sa"), (sb, "sb")):
@@ -183,7 +187,8 @@ def gemm(a, sa, b, sb, out_dtype=torch.bfloat16, b_tile: bool = False, out=None,
     _need(out, (torch.bfloat16, torch.float32), "out")
     _check(load().fp8_blockscaled_gemm(_ptr(a), _ptr(sa), _ptr(b), _ptr(sb), _ptr(out),
                                        _out_code(out.dtype), M, N, K,
-                                       B_TILE1x128 if b_tile else 0, _stream(stream)),
+                                       (B_TILE1x128 if b_tile else 0) | (WHOLE_K if whole_k else 0),
+                                       _stream(stream)),
            "fp8_blockscaled_gemm")
     return out
 

@@ -133,7 +133,7 @@ bool have_device() { return device_sm_count() > 0; }
 
 extern "C" {
 
-int fp8fg_abi_version(void) { return 4; }
+int fp8fg_abi_version(void) { return 5; }
 
 const char* fp8fg_status_string(fp8fg_status status) {
   switch (status) {
@@ -201,8 +201,10 @@ fp8fg_status fp8_weight_quant(const void* w, fp8fg_dtype w_dtype, int64_t N, int
 fp8fg_status fp8_blockscaled_gemm(const uint8_t* a, const float* sa, const uint8_t* b,
                                   const float* sb, void* c, fp8fg_dtype c_dtype, int64_t M,
                                   int64_t N, int64_t K, unsigned flags, void* stream) {
-  if (!valid_dtype(c_dtype) || (flags & ~FP8FG_B_TILE1x128) != 0 || M < 0 || N < 0 || K < 0)
+  if (!valid_dtype(c_dtype) || (flags & ~(FP8FG_B_TILE1x128 | FP8FG_WHOLE_K)) != 0 || M < 0 ||
+      N < 0 || K < 0)
     return FP8FG_ERR_INVALID_ARG;
+  if ((flags & FP8FG_B_TILE1x128) && (flags & FP8FG_WHOLE_K)) return FP8FG_ERR_INVALID_ARG;
   if (b == nullptr || sb == nullptr || (M > 0 && (a == nullptr || sa == nullptr || c == nullptr)))
     return FP8FG_ERR_INVALID_ARG;
   const bool b_tile = (flags & FP8FG_B_TILE1x128) != 0;
@@ -214,7 +216,8 @@ fp8fg_status fp8_blockscaled_gemm(const uint8_t* a, const float* sa, const uint8
     return FP8FG_ERR_MISALIGNED;
   if (M == 0) return FP8FG_OK;
   if (!have_device()) return FP8FG_ERR_CUDA;
-  return launch_gemm(a, sa, b, sb, c, c_dtype, M, N, K, b_tile, as_stream(stream));
+  return launch_gemm(a, sa, b, sb, c, c_dtype, M, N, K, b_tile, (flags & FP8FG_WHOLE_K) != 0,
+                     as_stream(stream));
 }
 
 fp8fg_status fp8_blockscaled_gemm_quant(const uint8_t* a, const float* sa, const uint8_t* b,

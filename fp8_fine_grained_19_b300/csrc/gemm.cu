@@ -79,6 +79,10 @@ constexpr uint32_t IDESC = idesc_e4m3_f32(BM, BN);
 constexpr int EPI_STORE = 0;    // C in BF16 or FP32
 constexpr int EPI_QUANT = 1;    // dense: C as 1x128 E4M3 tiles + scales
 constexpr int EPI_SWIGLU = 2;   // grouped: h = silu(gate) * up as 1x128 E4M3 tiles + scales
+// Study mode (dense, block path): no per-slice promotion.  All of K accumulates
+// in one TMEM buffer per tile and is scaled once by per-tensor scales
+// sa[0] * sb[0]; this measures the tensor core's own FP8 accumulation.
+constexpr int EPI_WHOLEK = 3;
 
 struct GemmParams {
   const float* sa;        // [rows, nkb]
@@ -306,14 +310,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       int stage = 0;
       uint32_t phase = 0;
       uint32_t it = 0;                              // slice counter (TMEM buffers)
+      uint32_t tcount = 0;                          // tile counter (study mode buffers)
       bool ok = true;
-      for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+      for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x, ++tcount) {
         for (int kb = 0; kb < nkb; ++kb, ++it) {
-          const uint32_t buf = it & 1, bpar = (it >> 1) & 1;
+          const uint32_t ix = EPI == EPI_WHOLEK ? tcount : it;
+          const uint32_t buf = ix & 1, bpar = (ix >> 1) & 1;
           int got = 0;
           if (lane == 0)
-            got = mbar_wait(smem_u32(&sm.tempty_bar[buf]), bpar ^ 1, p.wait_limit, abort_flag,
-                            p.status) &&
+            got = (EPI != EPI_WHOLEK || kb == 0
+                       ? mbar_wait(smem_u32(&sm.tempty_bar[buf]), bpar ^ 1, p.wait_limit,
+                                   abort_flag, p.status)
+                       : true) &&
                   mbar_wait(smem_u32(&sm.full_bar[stage]), phase, p.wait_limit, abort_flag,
                             p.status);
           if (!__shfl_sync(0xFFFFFFFFu, got, 0)) {
@@ -327,9 +335,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
           for (int k = 0; k < BK / 32; ++k)
             mma_f8_elect(d, smem_desc_sw128(a0 + 32 * k), smem_desc_sw128(b0 + 32 * k), IDESC,
-                         k > 0 ? 1u : 0u);
+                         k > 0 || (EPI == EPI_WHOLEK && kb > 0) ? 1u : 0u);
           mma_commit_elect(smem_u32(&sm.empty_bar[stage]));
-          mma_commit_elect(smem_u32(&sm.tfull_bar[buf]));
+          if (EPI != EPI_WHOLEK || kb == nkb - 1) mma_commit_elect(smem_u32(&sm.tfull_bar[buf]));
           if (++stage == STAGES) { stage = 0; phase ^= 1; }
         }
       }
@@ -350,6 +358,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const int n_blocks = p.N / 128;                 // block-mode scale rows per expert
     const uint32_t lane_taddr = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + half * 128;
     uint32_t it = 0;
+    uint32_t tcount = 0;                            // tile counter (study mode buffers)
     bool staged = false;                            // a store of this warp may still read cst
     bool ok = true;
     for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
@@ -436,6 +445,29 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           ok = false;
           break;
         }
+      } else if constexpr (EPI == EPI_WHOLEK) {
+        // the whole K sum of this tile sits in buffer tcount % 2: scale it once
+        const float s = __ldg(p.sa) * __ldg(p.sb);
+        const uint64_t s2 = pack2(__float_as_uint(s), __float_as_uint(s));
+        const uint32_t buf = tcount & 1, bpar = (tcount >> 1) & 1;
+        ++tcount;
+        if (!mbar_wait(smem_u32(&sm.tfull_bar[buf]), bpar, p.wait_limit, abort_flag, p.status)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t taddr = lane_taddr + buf * BN;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t r[32];
+          tmem_ld_32cols(taddr + c * 32, r);
+          tmem_ld_wait();
+#pragma unroll
+          for (int j = 0; j < 16; ++j) fma2(acc[c * 16 + j], pack2(r[2 * j], r[2 * j + 1]), s2);
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&sm.tempty_bar[buf]));
       } else {
         // SwiGLU: columns 64..127 of the half are up rows, whose block scale
         // lies I/128 blocks after the gate block
@@ -749,11 +781,13 @@ cudaError_t set_smem_attr() {
 
 fp8fg_status launch_gemm(const uint8_t* a, const float* sa, const uint8_t* b, const float* sb,
                          void* c, fp8fg_dtype ct, int64_t M, int64_t N, int64_t K, bool b_tile,
-                         cudaStream_t st) {
+                         bool whole_k, cudaStream_t st) {
   CUtensorMap mA, mB, mC;
   if (!make_maps(&mA, &mB, a, M, b, 0, N, K) || !make_c_map(&mC, c, ct, M, N))
     return FP8FG_ERR_CUDA;
-  if ((b_tile ? set_smem_attr<false, true>() : set_smem_attr<false, false>()) != cudaSuccess)
+  if ((b_tile ? set_smem_attr<false, true>()
+              : whole_k ? set_smem_attr<false, false, EPI_WHOLEK>() : set_smem_attr<false, false>()) !=
+      cudaSuccess)
     return FP8FG_ERR_CUDA;
   GemmParams p{};
   p.sa = sa;
@@ -775,6 +809,9 @@ fp8fg_status launch_gemm(const uint8_t* a, const float* sa, const uint8_t* b, co
   const int grid = tiles < device_sm_count() ? tiles : device_sm_count();
   if (b_tile)
     blockscaled_gemm_kernel<false, true, EPI_STORE><<<grid, NUM_THREADS, kSmemBytes, st>>>(mA, mB, mC, p);
+  else if (whole_k)
+    blockscaled_gemm_kernel<false, false, EPI_WHOLEK><<<grid, NUM_THREADS, kSmemBytes, st>>>(mA, mB, mC,
+                                                                                           p);
   else
     blockscaled_gemm_kernel<false, false, EPI_STORE><<<grid, NUM_THREADS, kSmemBytes, st>>>(mA, mB, mC, p);
   return cudaGetLastError() == cudaSuccess ? FP8FG_OK : FP8FG_ERR_CUDA;

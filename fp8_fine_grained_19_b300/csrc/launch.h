@@ -26,9 +26,10 @@ cudaError_t launch_weight_quant(const void* w, fp8fg_dtype wt, int64_t N, int64_
                                 float* s, uint8_t* qt, float* st_, bool pow2, cudaStream_t st);
 
 // Dense block-scaled GEMM (b_tile: B carries 1x128 tile scales).
+// whole_k: study mode, all of K accumulated in the tensor core, per-tensor scales.
 fp8fg_status launch_gemm(const uint8_t* a, const float* sa, const uint8_t* b, const float* sb,
                          void* c, fp8fg_dtype ct, int64_t M, int64_t N, int64_t K, bool b_tile,
-                         cudaStream_t st);
+                         bool whole_k, cudaStream_t st);
 // Dense block-scaled GEMM whose result leaves as 1x128 E4M3 tiles (q, s).
 fp8fg_status launch_gemm_quant(const uint8_t* a, const float* sa, const uint8_t* b,
                                const float* sb, uint8_t* q, float* s, int64_t M, int64_t N,

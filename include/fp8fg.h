@@ -53,6 +53,7 @@ typedef enum { FP8FG_BF16 = 0, FP8FG_F32 = 1 } fp8fg_dtype;
 #define FP8FG_POW2 1u          /* scales rounded up to an integral power of 2 */
 #define FP8FG_TRANSPOSE 2u     /* act_quant: 128x1 tiles, transposed output */
 #define FP8FG_B_TILE1x128 4u   /* GEMM: B carries 1x128 tile scales [N, K/128] */
+#define FP8FG_WHOLE_K 8u       /* GEMM study mode: no per-128-K promotion (see below) */
 
 /*
  * fp8_act_quant -- online 1x128 tile quantisation of activations to E4M3.
@@ -126,6 +127,14 @@ fp8fg_status fp8_weight_quant(const void* w, fp8fg_dtype w_dtype, int64_t N, int
  * over K group kb; each P_kb is scaled and added into an FP32 accumulator; the
  * output is rounded once (RNE to BF16, or stored as FP32).
  * M >= 0 arbitrary (0: nothing launched); N >= 16; K >= 128.
+ *
+ * FP8FG_WHOLE_K (study mode, not with FP8FG_B_TILE1x128): the promotion the
+ * pages prescribe is switched off.  All of K accumulates inside the tensor
+ * core (one TMEM accumulator per tile) and the result is scaled once by
+ * sa[0] * sb[0], i.e. per-tensor scales; sa and sb still have their usual
+ * shapes but only their first element is read.  It measures the accumulation
+ * error the promotion exists to avoid (page 2, passage on the limited
+ * accumulation precision of FP8 tensor-core GEMMs and Figure 6).
  */
 fp8fg_status fp8_blockscaled_gemm(const uint8_t* a, const float* sa, const uint8_t* b,
                                   const float* sb, void* c, fp8fg_dtype c_dtype, int64_t M,

@@ -1,0 +1,67 @@
+"""How much does the promotion buy on B300?  (page 2, inprokorea.com free #735329:
+accumulation-precision passage and Figure 6; next-row study.)
+
+Operands of the K-sweep workload (2048 x 2048 x K, N(0,1) with Student-t
+outliers) are quantised with ONE scale per tensor, so that the promoted GEMM
+(every 128-K partial scaled and added in FP32) and the study mode without
+promotion (all of K inside the tensor core, FP8FG_WHOLE_K) compute the same
+mathematical sum; the oracle gives it exactly on sampled rows.  The 14-bit
+aligned-accumulation model of the pages' H800 statement runs on a smaller
+sample for comparison.  The test prints one line per K (run with -s) and
+asserts only what must hold: the promoted result within the FP32 tolerance,
+and both errors finite and below 5 %.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from oracle import accumulation, e4m3
+from tests import helpers as H
+
+pytestmark = pytest.mark.gpu
+
+
+def _per_tensor(x):
+    a = np.float32(np.abs(x).max())
+    s = np.float32(a / np.float32(448.0))
+    m = np.float32(np.float32(448.0) / a)
+    return e4m3.encode((x * m).astype(np.float32)), s
+
+
+@pytest.mark.parametrize("K", [4096, 8192, 16384])
+def test_whole_k_accumulation_error(cuda_lib, K):
+    case = synth.dense_case(f"ksweep{K}")
+    x, w = H.f32(case.x()), H.f32(case.w())
+    qa, s_a = _per_tensor(x)
+    qb, s_b = _per_tensor(w)
+    M, N = qa.shape[0], qb.shape[0]
+    sa = np.full((M, K // 128), s_a, np.float32)
+    sb = np.full((N // 128, K // 128), s_b, np.float32)
+    d = [H.to_dev(v) for v in (qa, sa, qb, sb)]
+    promoted = cuda_lib.gemm(*d, out_dtype=torch.float32).cpu().numpy()
+    whole = cuda_lib.gemm(*d, out_dtype=torch.float32, whole_k=True).cpu().numpy()
+    rows = np.array([0, 1, 517, 1024, 2047])
+    ref = oracle.gemm(qa[rows], sa[rows], qb, sb)
+    scale = np.abs(ref).max()
+
+    def errs(c):
+        e = c.astype(np.float64) - ref
+        return np.linalg.norm(e) / np.linalg.norm(ref), np.abs(e).max() / scale
+
+    p_norm, p_max = errs(promoted[rows])
+    w_norm, w_max = errs(whole[rows])
+    # the aligned 14-bit model on 2 rows x 64 columns
+    A = e4m3.decode(qa[rows[:2]]) * np.float64(s_a)
+    B = e4m3.decode(qb[:64]) * np.float64(s_b)
+    m14 = accumulation.aligned_dot_rows(A, B, bits=14, group=32)
+    r14 = ref[:2, :64]
+    e14 = np.linalg.norm(m14 - r14) / np.linalg.norm(r14)
+    e14_max = np.abs(m14 - r14).max() / np.abs(r14).max()
+    print(f"\nK={K}: promoted normwise {p_norm:.2e} max/|C|max {p_max:.2e}; "
+          f"whole-K (B300 tensor core) normwise {w_norm:.2e} max/|C|max {w_max:.2e}; "
+          f"14-bit model normwise {e14:.2e} max/|C|max {e14_max:.2e}")
+    assert p_norm <= 1e-5
+    assert np.isfinite(w_norm) and w_norm < 0.05 and w_max < 0.05

@@ -40,7 +40,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_abi_version_and_status_strings(lib):
-    assert lib.fp8fg_abi_version() == 4
+    assert lib.fp8fg_abi_version() == 5
     for code in range(7):
         assert fp8.status_string(code)
     assert "unknown" in fp8.status_string(99)
@@ -91,6 +91,7 @@ def test_gemm_rejections(lib):
     ok = (A16, A16, A16, A16, A16)
     assert f(*ok, 2, 128, 256, 256, 0, None) == fp8.ERR_INVALID_ARG                   # dtype
     assert f(*ok, 0, 128, 256, 256, 16, None) == fp8.ERR_INVALID_ARG                  # flag
+    assert f(*ok, 0, 128, 256, 256, fp8.WHOLE_K | fp8.B_TILE1x128, None) == fp8.ERR_INVALID_ARG
     assert f(None, A16, A16, A16, A16, 0, 128, 256, 256, 0, None) == fp8.ERR_INVALID_ARG
     assert f(*ok, 0, 128, 256, 200, 0, None) == fp8.ERR_UNSUPPORTED_SHAPE             # K % 128
     assert f(*ok, 0, 128, 200, 256, 0, None) == fp8.ERR_UNSUPPORTED_SHAPE             # N % 128
