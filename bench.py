@@ -198,10 +198,6 @@ def run_ours(args, rank, world):
         ev[0].record(stream); act(x); ev[1].record(stream); wq(w); ev[2].record(stream)
         mm(); ev[3].record(stream)
 
-    def barrier():
-        if world > 1:
-            torch.distributed.barrier()
-
     for _ in range(max(args.warmup, 3)):
         step()
     torch.cuda.synchronize()
@@ -210,7 +206,7 @@ def run_ours(args, rank, world):
 
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    barrier()
+    barrier(world)
     torch.cuda.synchronize()
     with ClockSampler(dev.index) as clk:
         t0.record(stream)
@@ -218,12 +214,8 @@ def run_ours(args, rank, world):
             step(evs[i])
         t1.record(stream)
         torch.cuda.synchronize()
-    barrier()
-    ms = t0.elapsed_time(t1)
-    if world > 1:
-        tt = torch.tensor([ms], device=dev, dtype=torch.float64)
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        ms = float(tt.item())
+    barrier(world)
+    ms = max_over_ranks(t0.elapsed_time(t1), world, dev)
     status = fp8.device_status()
     if status != fp8.OK:
         raise RuntimeError(f"device status {fp8.status_string(status)}")
@@ -245,20 +237,16 @@ def run_ours(args, rank, world):
 
         e2e_step()
         torch.cuda.synchronize()
-        barrier()
+        barrier(world)
         a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a0.record(stream)
         for _ in range(n2):
             e2e_step()
         a1.record(stream)
         torch.cuda.synchronize()
-        barrier()
-        ms2 = a0.elapsed_time(a1)
-        if world > 1:
-            tt = torch.tensor([ms2], device=dev, dtype=torch.float64)
-            torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-            ms2 = float(tt.item())
-        e2e = {"value": round(world * n2 * FLOPS / (ms2 * 1e-3) / 1e12, 3), "unit": "TFLOP/s",
+        barrier(world)
+        ms2 = max_over_ranks(a0.elapsed_time(a1), world, dev)
+        e2e = {"value": round(job_rate(world, n2 * FLOPS, ms2) / 1e12, 3), "unit": "TFLOP/s",
                "steps": n2,
                "h2d_bytes_per_step": x_h.numel() * 2 + w_h.numel() * 2,
                "d2h_bytes_per_step": c_h.numel() * 2}
@@ -278,7 +266,7 @@ def run_ours(args, rank, world):
     wq_gbs = wq_bytes / (t_wq * 1e-3) / 1e9
     out = {
         "metric": METRIC,
-        "value": round(world * args.steps * FLOPS / (ms * 1e-3) / 1e12, 3),
+        "value": round(job_rate(world, args.steps * FLOPS, ms) / 1e12, 3),
         "unit": "TFLOP/s",
         "n_gpus": world, "steps": args.steps, "warmup": max(args.warmup, 3),
         "ms_per_step": round(ms / args.steps, 5),
@@ -315,7 +303,29 @@ def run_ours(args, rank, world):
 
 
 # ---------------------------------------------------- other workloads
-def _timed_loop(ops, steps, warmup, stream, dev):
+def barrier(world: int) -> None:
+    """All ranks meet (no-op on one process)."""
+    if world > 1:
+        import torch
+        torch.distributed.barrier()
+
+
+def max_over_ranks(ms: float, world: int, device) -> float:
+    """The job's time: the slowest rank's, over the default process group."""
+    if world <= 1:
+        return ms
+    import torch
+    tt = torch.tensor([ms], device=device, dtype=torch.float64)
+    torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+    return float(tt.item())
+
+
+def job_rate(world: int, units_per_rank: float, ms: float) -> float:
+    """Whole-job throughput: every rank's units over the job's time (units/s)."""
+    return world * units_per_rank / (ms * 1e-3)
+
+
+def _timed_loop(ops, steps, warmup, stream, dev, world=1):
     """Run `ops` (list of (name, fn)) back to back `steps` times after `warmup`
     untimed steps; CUDA events around the whole region and around every op."""
     import torch
@@ -327,6 +337,7 @@ def _timed_loop(ops, steps, warmup, stream, dev):
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(ops) + 1)]
            for _ in range(steps)]
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
     torch.cuda.synchronize()
     with ClockSampler(dev.index) as clk:
         t0.record(stream)
@@ -337,9 +348,10 @@ def _timed_loop(ops, steps, warmup, stream, dev):
             evs[i][len(ops)].record(stream)
         t1.record(stream)
         torch.cuda.synchronize()
+    barrier(world)
     per = {name: statistics.mean(e[j].elapsed_time(e[j + 1]) for e in evs)
            for j, (name, _) in enumerate(ops)}
-    return t0.elapsed_time(t1), per, clk.summary()
+    return max_over_ranks(t0.elapsed_time(t1), world, dev), per, clk.summary()
 
 
 def run_workload(args, rank, world):
@@ -542,11 +554,12 @@ def run_workload(args, rank, world):
                 "l2": "working set 2-4x smaller than L2 for K <= 8192: these times include L2 hits"}
 
     steps = args.steps
-    total_ms, per, clocks = _timed_loop([(n, f) for n, f, _, _ in ops], steps, args.warmup, stream, dev)
+    total_ms, per, clocks = _timed_loop([(n, f) for n, f, _, _ in ops], steps, args.warmup, stream, dev,
+                                        world)
     extra = []
     if args.workload == "moe":
         _, per_c, _ = _timed_loop([(n, f) for n, f, _, _ in compare_ops], max(steps // 4, 5), args.warmup,
-                                  stream, dev)
+                                  stream, dev, world)
         per.update(per_c)
         extra = compare_ops
     status = fp8.device_status()
@@ -588,7 +601,7 @@ def run_workload(args, rank, world):
     cfg = dict(desc)
     cfg["parallelism"] = f"{world} independent replica(s)"
     return {
-        "metric": METRIC, "value": round(world * steps * gemm_flops / (total_ms * 1e-3) / 1e12, 3),
+        "metric": METRIC, "value": round(job_rate(world, steps * gemm_flops, total_ms) / 1e12, 3),
         "unit": "TFLOP/s", "n_gpus": world, "steps": steps, "warmup": max(args.warmup, 3),
         "ms_per_step": round(total_ms / steps, 5), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "e4m3 x e4m3 -> f32 accumulate", "data": "synthetic",
