@@ -24,6 +24,7 @@ import argparse
 import hashlib
 import json
 import os
+import re
 import statistics
 import sys
 import threading
@@ -70,9 +71,13 @@ def peaks():
 
 
 def src_hash(paths) -> str:
+    """Hash of the kernel sources' code: comments and whitespace do not count."""
     h = hashlib.sha256()
     for p in paths:
-        h.update(open(os.path.join(ROOT, p), "rb").read())
+        src = open(os.path.join(ROOT, p)).read()
+        src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+        src = re.sub(r"//[^\n]*", "", src)
+        h.update(re.sub(r"\s+", "", src).encode())
     return h.hexdigest()[:16]
 
 

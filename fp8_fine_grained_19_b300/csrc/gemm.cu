@@ -33,6 +33,13 @@
 // tensor pipe idles meanwhile.  The grouped kernel keeps per-thread row stores,
 // masked at each expert's end: with the staging code its K loop no longer
 // fits the promotion warps' registers and spills (measured 35% slower).
+// Output modes (template EPI): EPI_STORE writes C in BF16 or FP32; EPI_QUANT
+// (dense) quantises each thread's 128 columns of its row -- one 1x128 tile --
+// with the activation quantiser's rules and stores codes through the same
+// staging; EPI_SWIGLU (grouped) loads each B stage as gate/up/gate/up 64-row
+// boxes so that a thread holds g and u of the same 64 outputs, forms
+// h = silu(g) * u and stores h's codes and power-of-2 scales; EPI_WHOLEK is a
+// study mode that accumulates all of K in TMEM with per-tensor scales.
 // Tiles are visited in groups of 16 M-tiles (all N-tiles of a group before the
 // next), so a group's A rows stay in L2 while B streams once per group.
 // Every pipeline wait is bounded (FP8FG_ERR_TIMEOUT, see device_common.cuh).

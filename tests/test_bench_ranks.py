@@ -61,3 +61,15 @@ def test_single_process_helpers_need_no_process_group():
     b.barrier(1)
     assert b.max_over_ranks(3.5, 1, torch.device("cpu")) == 3.5
     assert b.job_rate(1, 10.0, 100.0) == pytest.approx(100.0)
+
+
+def test_source_hash_ignores_comments_but_not_code(tmp_path):
+    b = _bench()
+    a = tmp_path / "a.cu"
+    c = tmp_path / "c.cu"
+    d = tmp_path / "d.cu"
+    a.write_text("// header\nint f(int x) { return x + 1; }  /* tail */\n")
+    c.write_text("// another header\n\nint f(int x) {\n  return x + 1;  // same code\n}\n")
+    d.write_text("int f(int x) { return x + 2; }\n")
+    assert b.src_hash([str(a)]) == b.src_hash([str(c)])
+    assert b.src_hash([str(a)]) != b.src_hash([str(d)])
