@@ -74,3 +74,27 @@ def test_whole_k_accumulation_error(cuda_lib, K):
           f"({', '.join(f'{b}:{e:.1e}' for b, e in fits.items())})")
     assert p_norm <= 1e-5
     assert np.isfinite(w_norm) and w_norm < 0.05 and w_max < 0.05
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 128, 256), (129, 384, 640), (300, 256, 1152)])
+def test_whole_k_mode_small_ragged_shapes(cuda_lib, M, N, K):
+    # the study mode on ragged shapes: one scale per tensor (only sa[0, 0] and
+    # sb[0, 0] are read), rows past M untouched, result within FP32-level
+    # accumulation error of the exact sum
+    g = np.random.default_rng(M + N + K)
+    qa = e4m3.encode((g.standard_normal((M, K)) * 50).astype(np.float32))
+    qb = e4m3.encode((g.standard_normal((N, K)) * 50).astype(np.float32))
+    s_a, s_b = np.float32(0.0123), np.float32(3.5)
+    sa = np.full((M, K // 128), s_a, np.float32)
+    sb = np.full((N // 128, K // 128), s_b, np.float32)
+    sa_dev = H.to_dev(sa.copy())
+    sa_dev.view(-1)[1:] = 7.0                      # only the first scale may be read
+    sb_dev = H.to_dev(sb.copy())
+    sb_dev.view(-1)[1:] = 7.0
+    raw, out = H.guarded_empty((M, N), torch.float32)
+    cuda_lib.gemm(H.to_dev(qa), sa_dev, H.to_dev(qb), sb_dev, out_dtype=torch.float32,
+                  whole_k=True, out=out)
+    torch.cuda.synchronize()
+    assert H.guards_intact(raw), "write outside the output"
+    ref = oracle.gemm(qa, sa, qb, sb)
+    assert H.normwise_rel_err(out, ref) <= 1e-5
