@@ -258,6 +258,7 @@ fp8fg_status fp8_grouped_gemm(const uint8_t* a, const float* sa, const int32_t* 
   if (!aligned16(a) || !aligned16(sa) || !aligned16(b) || !aligned16(sb) || !aligned16(c) ||
       (reinterpret_cast<uintptr_t>(offsets) & 3u) != 0)
     return FP8FG_ERR_MISALIGNED;
+  if (total_rows == 0) return FP8FG_OK;    // no rows: nothing to compute or write
   if (!have_device()) return FP8FG_ERR_CUDA;
   return launch_grouped_gemm(a, sa, offsets, E, total_rows, b, sb, c, c_dtype, N, K,
                              as_stream(stream));
@@ -279,6 +280,7 @@ fp8fg_status fp8_grouped_gemm_swiglu_quant(const uint8_t* a, const float* sa,
   if (!aligned16(a) || !aligned16(sa) || !aligned16(b) || !aligned16(sb) || !aligned16(q) ||
       !aligned16(s) || (reinterpret_cast<uintptr_t>(offsets) & 3u) != 0)
     return FP8FG_ERR_MISALIGNED;
+  if (total_rows == 0) return FP8FG_OK;    // no rows: nothing to compute or write
   if (!have_device()) return FP8FG_ERR_CUDA;
   return launch_grouped_swiglu_quant(a, sa, offsets, E, total_rows, b, sb, q, s, N, K,
                                      (flags & FP8FG_POW2) != 0, as_stream(stream));

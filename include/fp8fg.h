@@ -174,7 +174,8 @@ fp8fg_status fp8_blockscaled_gemm_quant(const uint8_t* a, const float* sa, const
  *          checked on the device (FP8FG_ERR_BAD_OFFSETS, nothing written).
  * b        [E, N, K] codes; sb [E, N/128, K/128] FP32 (128x128 blocks).
  * c        [total_rows, N] BF16 or FP32.  Rows of empty experts: none.
- * Requires 1 <= E <= 1024, N % 128 == 0; flags must be 0.
+ * Requires 1 <= E <= 1024, N % 128 == 0; flags must be 0.  total_rows == 0:
+ * nothing is launched (a, sa and c may be null; offsets are not read).
  */
 fp8fg_status fp8_grouped_gemm(const uint8_t* a, const float* sa, const int32_t* offsets,
                               int32_t E, int64_t total_rows, const uint8_t* b, const float* sb,
@@ -201,6 +202,7 @@ fp8fg_status fp8_grouped_gemm(const uint8_t* a, const float* sa, const int32_t* 
  * activation quantiser's rules apply, power-of-2 scales with FP8FG_POW2 (the
  * pages' choice for this tensor).
  * Requires 1 <= E <= 1024, N % 256 == 0, K % 128 == 0; flags within FP8FG_POW2.
+ * total_rows == 0: nothing is launched (a, sa, q and s may be null).
  */
 fp8fg_status fp8_grouped_gemm_swiglu_quant(const uint8_t* a, const float* sa,
                                            const int32_t* offsets, int32_t E, int64_t total_rows,

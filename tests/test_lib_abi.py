@@ -122,6 +122,7 @@ def test_grouped_rejections(lib):
     assert f(*args(E=2000)) == fp8.ERR_UNSUPPORTED_SHAPE
     assert f(*args(N=200)) == fp8.ERR_UNSUPPORTED_SHAPE
     assert f(*args(off=A16 + 2)) == fp8.ERR_MISALIGNED
+    assert f(None, None, A16, 4, 0, A16, A16, None, 0, 256, 256, 0, None) == fp8.OK  # no rows
 
 
 def test_grouped_swiglu_rejections(lib):
@@ -137,6 +138,8 @@ def test_grouped_swiglu_rejections(lib):
     assert f(*args(E=2000)) == fp8.ERR_UNSUPPORTED_SHAPE
     assert f(*args(off=A16 + 2)) == fp8.ERR_MISALIGNED
     assert f(*args(s=MIS)) == fp8.ERR_MISALIGNED
+    # no rows: nothing launched, null row buffers accepted (no device needed)
+    assert f(None, None, A16, 4, 0, A16, A16, None, None, 512, 256, fp8.POW2, None) == fp8.OK
 
 
 def test_selftest_rejects_bad_limit(lib):
