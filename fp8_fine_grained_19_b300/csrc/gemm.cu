@@ -30,9 +30,9 @@
 // tensor map's 64-byte swizzle and writes it with one TMA tile store, which
 // clips at the matrix bounds.  Per-thread row stores (16 bytes into 32
 // different rows per instruction) take two to three times as long, and the
-// tensor pipe idles meanwhile.  The grouped kernel keeps per-thread row stores,
-// masked at each expert's end: with the staging code its K loop no longer
-// fits the promotion warps' registers and spills (measured 35% slower).
+// tensor pipe idles meanwhile.  The grouped kernel does the same for warps
+// whose rows lie inside one expert, and per-thread row stores, masked at the
+// expert's end, for a warp that straddles it.
 // Output modes (template EPI): EPI_STORE writes C in BF16 or FP32; EPI_QUANT
 // (dense) quantises each thread's 128 columns of its row -- one 1x128 tile --
 // with the activation quantiser's rules and stores codes through the same
@@ -70,11 +70,19 @@ constexpr int REGS_LAUNCH = 168;
 constexpr int REGS_PRODUCER = 56;
 constexpr int REGS_EPILOGUE = 224;
 static_assert(2 * REGS_EPILOGUE + REGS_PRODUCER <= 3 * REGS_LAUNCH, "register split");
-// The grouped SwiGLU kernel spills at the 224/56 split (the report does not
-// say where); at 208/88 it compiles without spills.
+// The grouped kernels spill at the 224/56 split (their TMA/MMA warpgroup needs
+// more than 56 registers for the expert-tile lookup): the plain grouped kernel
+// runs at 184/136 and the SwiGLU kernel at 208/88, both without spills.
 constexpr int SWIGLU_REGS_EPILOGUE = 208;
-constexpr int SWIGLU_REGS_PRODUCER = (3 * REGS_LAUNCH - 2 * SWIGLU_REGS_EPILOGUE) / 8 * 8;
-static_assert(2 * SWIGLU_REGS_EPILOGUE + SWIGLU_REGS_PRODUCER <= 3 * REGS_LAUNCH, "register split");
+constexpr int GROUPED_REGS_EPILOGUE = 184;
+__host__ __device__ constexpr int regs_epilogue(bool grouped, int epi) {
+  return epi == 2 ? SWIGLU_REGS_EPILOGUE : grouped ? GROUPED_REGS_EPILOGUE : REGS_EPILOGUE;
+}
+__host__ __device__ constexpr int regs_producer(bool grouped, int epi) {
+  return (3 * REGS_LAUNCH - 2 * regs_epilogue(grouped, epi)) / 8 * 8;
+}
+static_assert(2 * SWIGLU_REGS_EPILOGUE + regs_producer(true, 2) <= 3 * REGS_LAUNCH, "register split");
+static_assert(2 * GROUPED_REGS_EPILOGUE + regs_producer(true, 0) <= 3 * REGS_LAUNCH, "register split");
 constexpr int TMEM_COLS = 512;
 constexpr int GROUP_M = 16;
 constexpr int MAX_EXPERTS = 1024;
@@ -268,8 +276,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   const int nkb = p.nkb;
 
   if (warp >= NUM_EPI_WARPS) {
-    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(EPI == EPI_SWIGLU ? SWIGLU_REGS_PRODUCER
-                                                                             : REGS_PRODUCER));
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(regs_producer(GROUPED, EPI)));
     if (warp == PRODUCER_WARP) {
       // ------------------------------------------------------- TMA producer
       if (lane == 0) {
@@ -357,8 +364,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
   } else {
     // ------------------------------------------------ promotion + epilogue
-    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(EPI == EPI_SWIGLU ? SWIGLU_REGS_EPILOGUE
-                                                                             : REGS_EPILOGUE));
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(regs_epilogue(GROUPED, EPI)));
     const int quad = warp & 3;                      // TMEM lane quadrant
     const int half = warp >> 2;                     // N half of the tile
     const int tid_h = threadIdx.x & 127;            // index within the half's warpgroup
@@ -574,9 +580,57 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           }
         }
       } else if constexpr (GROUPED) {
-        // --- grouped: each thread stores its row segment (128 columns of its
-        // half); rows past the expert's end belong to the next expert
-        if (row_ok && half_ok) {
+        // --- grouped: a warp whose 32 rows lie inside the expert (or end at M,
+        // where the store clips) writes through the swizzled staging and TMA
+        // tile stores like the dense kernel; a warp whose rows run past the
+        // expert's end (the rows after belong to the next expert) stores its
+        // valid rows per thread.
+        const int wrow0 = tl.m0 + quad * 32;
+        const bool whole = wrow0 + 32 <= tl.row_end || tl.row_end == p.M;
+        if (half_ok && wrow0 < tl.row_end && whole) {
+          uint32_t wl = (warp << 8) | lane;
+          asm volatile("" : "+r"(wl));
+          const uint32_t cbuf = smem_u32(sm.cst[0]) + (wl >> 8) * CST_BYTES;
+          const uint32_t srow = cbuf + (wl & 31) * CST_ROW;
+          const uint32_t swz = ((wl & 31) >> 1) & 3;
+          const int W = p.c_f32 ? 16 : 32;        // columns per chunk
+#pragma unroll
+          for (int q = 0; q < 8; ++q) {
+            if (p.c_f32 || q < 4) {
+              if (staged) {
+                if (lane == 0) bulk_wait_read_all();
+                __syncwarp();
+              }
+#pragma unroll
+              for (int u = 0; u < 4; ++u) {
+                uint32_t w[4];
+                if (p.c_f32) {
+                  const uint64_t x0 = acc[8 * q + 2 * u], x1 = acc[8 * q + 2 * u + 1];
+                  w[0] = static_cast<uint32_t>(x0);
+                  w[1] = static_cast<uint32_t>(x0 >> 32);
+                  w[2] = static_cast<uint32_t>(x1);
+                  w[3] = static_cast<uint32_t>(x1 >> 32);
+                } else {
+#pragma unroll
+                  for (int i = 0; i < 4; ++i) {
+                    float lo, hi;
+                    unpack2(acc[(16 * q + 4 * u + i) & 63], lo, hi);
+                    const __nv_bfloat162 b2 = __floats2bfloat162_rn(lo, hi);
+                    w[i] = *reinterpret_cast<const uint32_t*>(&b2);
+                  }
+                }
+                sts_128(srow + ((u ^ swz) << 4), w[0], w[1], w[2], w[3]);
+              }
+              fence_proxy_async_smem();
+              __syncwarp();
+              if (lane == 0) {
+                tma_store_2d(&tmC, cbuf, col_h + q * W, wrow0);
+                bulk_commit();
+              }
+              staged = true;
+            }
+          }
+        } else if (row_ok && half_ok) {
           if (p.c_f32) {
             float* dst = static_cast<float*>(p.c) + static_cast<int64_t>(row) * p.N + col_h;
 #pragma unroll
