@@ -137,6 +137,7 @@ struct Smem {
   int abort_flag;
   int bad_offsets;
   int num_tiles;
+  float amx[2][4][32];            // SwiGLU: per-row tile amax of each half (warp pairs)
   int cum[MAX_EXPERTS + 1];       // grouped: tile prefix per expert
   int row0[MAX_EXPERTS + 1];      // grouped: copy of offsets
 };
@@ -555,29 +556,54 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
         // amax slots: [half][quad][lane]; the partner's slot is rewritten only
         // after the next tile's pair vote, which follows this read
-        float* am = reinterpret_cast<float*>(sm.cst[0]);
-        am[(half * 4 + quad) * 32 + lane] = amax;
+        sm.amx[half][quad][lane] = amax;
         bar_sync(3 + quad, 64);
-        amax = fmaxf(amax, am[((half ^ 1) * 4 + quad) * 32 + lane]);
-        if (row_ok) {
-          const Scale sc = scale_from_amax(amax, p.pow2_out != 0);
-          const int I = p.N / 2;
-          const int j0 = tl.n0 / 2;
-          if (half == 0) p.s_out[static_cast<int64_t>(row) * (I / 128) + j0 / 128] = sc.s;
+        amax = fmaxf(amax, sm.amx[half ^ 1][quad][lane]);
+        const Scale sc = scale_from_amax(amax, p.pow2_out != 0);
+        const int I = p.N / 2;
+        const int j0 = tl.n0 / 2;
+        if (half == 0 && row_ok) p.s_out[static_cast<int64_t>(row) * (I / 128) + j0 / 128] = sc.s;
+        // the row's 64 codes are one 64-byte staging row: a warp whose rows lie
+        // inside the expert (or end at M) writes them with one TMA tile store
+        const int wrow0 = tl.m0 + quad * 32;
+        const bool whole = wrow0 + 32 <= tl.row_end || tl.row_end == p.M;
+        uint32_t w[16];
+#pragma unroll
+        for (int i = 0; i < 4; ++i)               // 16 codes = outputs 16i .. 16i+15
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            float x0, x1, x2, x3;
+            unpack2(acc[8 * i + 2 * k], x0, x1);
+            unpack2(acc[8 * i + 2 * k + 1], x2, x3);
+            w[4 * i + k] = e4m3x2(__fmul_rn(x0, sc.m), __fmul_rn(x1, sc.m)) |
+                           (e4m3x2(__fmul_rn(x2, sc.m), __fmul_rn(x3, sc.m)) << 16);
+          }
+        if (whole && wrow0 < tl.row_end) {
+          uint32_t wl = (warp << 8) | lane;
+          asm volatile("" : "+r"(wl));
+          const uint32_t cbuf = smem_u32(sm.cst[0]) + (wl >> 8) * CST_BYTES;
+          const uint32_t srow = cbuf + (wl & 31) * CST_ROW;
+          const uint32_t swz = ((wl & 31) >> 1) & 3;
+          if (staged) {
+            if (lane == 0) bulk_wait_read_all();
+            __syncwarp();
+          }
+#pragma unroll
+          for (int u = 0; u < 4; ++u)
+            sts_128(srow + ((u ^ swz) << 4), w[4 * u], w[4 * u + 1], w[4 * u + 2], w[4 * u + 3]);
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_2d(&tmC, cbuf, j0 + 64 * half, wrow0);
+            bulk_commit();
+          }
+          staged = true;
+        } else if (row_ok) {
           uint8_t* dst = static_cast<uint8_t*>(p.c) + static_cast<int64_t>(row) * I + j0 + 64 * half;
 #pragma unroll
-          for (int i = 0; i < 4; ++i) {           // 16 codes = outputs 16i .. 16i+15
-            uint32_t w[4];
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-              float x0, x1, x2, x3;
-              unpack2(acc[8 * i + 2 * k], x0, x1);
-              unpack2(acc[8 * i + 2 * k + 1], x2, x3);
-              w[k] = e4m3x2(__fmul_rn(x0, sc.m), __fmul_rn(x1, sc.m)) |
-                     (e4m3x2(__fmul_rn(x2, sc.m), __fmul_rn(x3, sc.m)) << 16);
-            }
-            *reinterpret_cast<uint4*>(dst + 16 * i) = make_uint4(w[0], w[1], w[2], w[3]);
-          }
+          for (int i = 0; i < 4; ++i)
+            *reinterpret_cast<uint4*>(dst + 16 * i) =
+                make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
         }
       } else if constexpr (GROUPED) {
         // --- grouped: a warp whose 32 rows lie inside the expert (or end at M,
@@ -977,9 +1003,17 @@ fp8fg_status launch_grouped_swiglu_quant(const uint8_t* a, const float* sa,
   p.pow2_out = pow2 ? 1 : 0;
   p.wait_limit = wait_limit_cycles();
   p.status = device_status_word();
-  // the C map is not used in this mode; any valid map fills the parameter
+  // h codes [total_rows, N/2] stored by 32-row x 64-byte boxes from swizzled staging
+  CUtensorMap mQ;
+  const uint64_t dQ[2] = {static_cast<uint64_t>(N / 2),
+                          static_cast<uint64_t>(total_rows > 0 ? total_rows : 1)};
+  const uint64_t sQ[1] = {static_cast<uint64_t>(N / 2)};
+  const uint32_t boxQ[2] = {CST_ROW, 32};
+  if (!encode_tensor_map(&mQ, CU_TENSOR_MAP_DATA_TYPE_UINT8, q, 2, dQ, sQ, boxQ,
+                         CU_TENSOR_MAP_SWIZZLE_64B))
+    return FP8FG_ERR_CUDA;
   blockscaled_gemm_kernel<true, false, EPI_SWIGLU><<<device_sm_count(), NUM_THREADS, kSmemBytes,
-                                                     st>>>(mA, mB, mA, p);
+                                                     st>>>(mA, mB, mQ, p);
   return cudaGetLastError() == cudaSuccess ? FP8FG_OK : FP8FG_ERR_CUDA;
 }
 
