@@ -136,3 +136,71 @@ def check_quant_decisions(q_gpu, s_gpu, x_ref, err, pow2):
     step = (np.maximum(y, 2.0 ** -6) * 2.0 ** -3 + 2.0 ** -9) * so[:, :, None]
     assert np.all(np.abs(dq - xt) <= step + Et), "code off by more than one step"
     return float(sure.mean())
+
+
+def gemm_error_bound(qa, sa, qb, sb, b_tile=False) -> np.ndarray:
+    """Per-element bound on |C32 - C| for the promoted FP32 sum (float64 [M, N]).
+
+    C = sum_kb P_kb * s_kb is the oracle's exact result (s_kb = sa[m,kb] * sb(n,kb)).
+    The GPU forms each group's partial T_kb in the tensor core (FP32 accumulation
+    of four K=32 products into TMEM), rounds s_kb to FP32, and adds T_kb * s_kb
+    into an FP32 accumulator with one rounding per group (page 2,
+    inprokorea.com free #735329, promotion passage and Figure 6).  With
+    A1 = sum_kb |P_kb| s_kb and A2 = sum_kb s_kb sum_{k in kb} |a_k b_k|:
+      * group partials: |T_kb - P_kb| <= 16 * 2^-24 * sum_{k in kb} |a_k b_k|
+        (four accumulation steps, each allowed 4 units of 2^-24 of the group's
+        magnitude sum; B300 measured at 25-26 bits of accumulation);
+      * the scale product: 2^-24 |P_kb s_kb|;
+      * the FP32 accumulation: at most nkb roundings of 2^-24 of a running sum
+        bounded by A1.
+    Hence |C32 - C| <= (nkb + 1) 2^-24 A1 + 16 * 2^-24 A2 (second-order terms are
+    far below the first-order slack).  A single wrong element (a dropped group, a
+    wrong scale) misses it by orders of magnitude.
+    """
+    qa = np.asarray(qa)
+    qb = np.asarray(qb)
+    M, K = qa.shape
+    N = qb.shape[0]
+    nkb = K // 128
+    sa64 = np.asarray(sa, np.float64)
+    sb64 = np.asarray(sb, np.float64)
+    mag_a, mag_b = qa & 0x7F, qb & 0x7F          # |decode(c)| = decode(c & 0x7F) (no NaN codes)
+    A1 = np.zeros((M, N))
+    A2 = np.zeros((M, N))
+    for kb in range(nkb):
+        sl = slice(128 * kb, 128 * (kb + 1))
+        P = oracle.slice_partials(qa[:, sl], qb[:, sl])[0]
+        Q = oracle.slice_partials(mag_a[:, sl], mag_b[:, sl])[0]
+        sbk = sb64[:, kb] if b_tile else np.repeat(sb64[:, kb], 128)[:N]
+        s = sa64[:, kb][:, None] * sbk[None, :]
+        A1 += np.abs(P) * s
+        A2 += Q * s
+    return (nkb + 1) * 2.0 ** -24 * A1 + 16 * 2.0 ** -24 * A2
+
+
+def grouped_error_bound(qa, sa, offsets, qb, sb) -> np.ndarray:
+    """gemm_error_bound per expert over contiguous row groups (float64 [T, N])."""
+    off = np.asarray(offsets, np.int64)
+    out = np.zeros((np.asarray(qa).shape[0], np.asarray(qb).shape[1]))
+    for e in range(len(off) - 1):
+        r0, r1 = int(off[e]), int(off[e + 1])
+        if r1 > r0:
+            out[r0:r1] = gemm_error_bound(qa[r0:r1], np.asarray(sa)[r0:r1], qb[e], sb[e])
+    return out
+
+
+def assert_elementwise(c_gpu, c_ref: np.ndarray, bound32: np.ndarray, what: str = "") -> float:
+    """Every element of the GPU result within its bound (FP32 output), or within the
+    bound plus one BF16 rounding of the FP32 value (2^-8 of it, RNE) for BF16 output.
+    Returns the largest |error| / bound."""
+    is_bf16 = isinstance(c_gpu, torch.Tensor) and c_gpu.dtype == torch.bfloat16
+    g = c_gpu.detach().float().cpu().numpy().astype(np.float64) if isinstance(c_gpu, torch.Tensor) \
+        else np.asarray(c_gpu, np.float64)
+    bound = bound32 + (2.0 ** -8 * (np.abs(c_ref) + bound32) if is_bf16 else 0.0)
+    err = np.abs(g - c_ref)
+    bad = err > bound
+    if bad.any():
+        i = tuple(np.argwhere(bad)[0])
+        raise AssertionError(f"{what}: {int(bad.sum())} elements outside the per-element bound; "
+                             f"first at {list(i)}: gpu {g[i]!r} ref {c_ref[i]!r} bound {bound[i]!r}")
+    return float((err / np.maximum(bound, 1e-300)).max())

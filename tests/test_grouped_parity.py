@@ -45,6 +45,7 @@ def test_ragged_groups(cuda_lib, sizes, dtype):
     assert H.guards_intact(raw)
     ref = oracle.grouped_gemm(qa, sa, off, qb, sb)
     assert H.normwise_rel_err(out, ref) <= TOL[dtype]
+    H.assert_elementwise(out, ref, H.grouped_error_bound(qa, sa, off, qb, sb), f"ragged {sizes}")
 
 
 def test_single_expert_matches_dense_kernel(cuda_lib):
@@ -107,10 +108,12 @@ def test_small_routed_layer_full(cuda_lib):
     qu_r = qu_r.reshape(case.E, 2 * case.I, case.H)
     su_r = su_r.reshape(case.E, 2 * case.I // 128, case.H // 128)
     dev_off = H.to_dev(off)
+    ref = oracle.grouped_gemm(qa_r, sa_r, off, qu_r, su_r)
+    bound = H.grouped_error_bound(qa_r, sa_r, off, qu_r, su_r)
     for dtype in (torch.bfloat16, torch.float32):
         up = cuda_lib.grouped_gemm(qa, sa, dev_off, qu, su, out_dtype=dtype)
-        ref = oracle.grouped_gemm(qa_r, sa_r, off, qu_r, su_r)
         assert H.normwise_rel_err(up, ref) <= TOL[dtype]
+        H.assert_elementwise(up, ref, bound, f"small routed up {dtype}")
     # down projection from a drawn h (power-of-2 scales)
     h = synth.swiglu_like_bf16((case.rows, case.I), case.seed)
     qh, sh = cuda_lib.act_quant(h.cuda(), pow2=True)
@@ -122,9 +125,11 @@ def test_small_routed_layer_full(cuda_lib):
     down = cuda_lib.grouped_gemm(qh, sh, dev_off, qd.view(case.E, case.H, case.I),
                                  sd.view(case.E, case.H // 128, case.I // 128),
                                  out_dtype=torch.float32)
-    ref = oracle.grouped_gemm(qh_r, sh_r, off, qd_r.reshape(case.E, case.H, case.I),
-                              sd_r.reshape(case.E, case.H // 128, case.I // 128))
+    qd3 = qd_r.reshape(case.E, case.H, case.I)
+    sd3 = sd_r.reshape(case.E, case.H // 128, case.I // 128)
+    ref = oracle.grouped_gemm(qh_r, sh_r, off, qd3, sd3)
     assert H.normwise_rel_err(down, ref) <= TOL[torch.float32]
+    H.assert_elementwise(down, ref, H.grouped_error_bound(qh_r, sh_r, off, qd3, sd3), "small routed down")
 
 
 def test_full_routed_layer_sampled_experts(cuda_lib):
@@ -158,3 +163,5 @@ def test_full_routed_layer_sampled_experts(cuda_lib):
         toks = r["token_of_row"][rows]
         ref = oracle.gemm(qx_r[toks], sx_r[toks], qe_r, se_r)
         assert H.normwise_rel_err(up[rows], ref) <= TOL[torch.bfloat16], e
+        H.assert_elementwise(up[rows], ref, H.gemm_error_bound(qx_r[toks], sx_r[toks], qe_r, se_r),
+                             f"full routed up, expert {e}")

@@ -4,8 +4,9 @@ oracle.grouped_swiglu_quant: per expert, g and u are the gate and up halves of
 the promoted up-projection; h = silu(g) * u is quantised into 1x128 tiles with
 power-of-2 scales (page 2, inprokorea.com free #735329, power-of-2 passage).
 
-The GPU forms g and u as FP32 sums (each off by at most
-E = (nkb + 1) * 2^-24 * sum_kb |P_kb sa sb|) and h = g / (1 + expf(-g)) * u in
+The GPU forms g and u as FP32 sums (each off by at most the per-element bound E
+of tests/helpers.py, gemm_error_bound: the FP32 roundings of the promoted sum,
+including the tensor core's accumulation inside each 128-K group) and h = g / (1 + expf(-g)) * u in
 FP32 with the fast exponential and divide, whose documented bounds (2 + 1.173|x|
 ulp and 2 ulp) give silu a relative error of at most (4 + 1.2|g|) 2^-23; below
 g = -87 the divide returns zero, counted here as an error of |h|.  With
@@ -28,26 +29,10 @@ pytestmark = pytest.mark.gpu
 FINITE = np.array([c for c in range(256) if (c & 0x7F) != 0x7F], dtype=np.uint8)
 
 
-def _abs_grouped(qa, sa, off, qb, sb):
-    """sum_kb |P_kb| sa sb per element of the grouped product (float64 [T, N])."""
-    T, N = qa.shape[0], qb.shape[1]
-    out = np.zeros((T, N))
-    for e in range(len(off) - 1):
-        r0, r1 = int(off[e]), int(off[e + 1])
-        if r1 == r0:
-            continue
-        P = np.abs(oracle.slice_partials(qa[r0:r1], qb[e]))
-        for kb in range(P.shape[0]):
-            out[r0:r1] += (P[kb] * sa[r0:r1, kb].astype(np.float64)[:, None]
-                           * np.repeat(sb[e][:, kb].astype(np.float64), 128)[None, :])
-    return out
-
-
 def _h_error_bound(qa, sa, off, qb, sb):
-    nkb = qa.shape[1] // 128
     I = qb.shape[1] // 2
     C = oracle.grouped_gemm(qa, sa, off, qb, sb)
-    E = (nkb + 1) * 2.0 ** -24 * _abs_grouped(qa, sa, off, qb, sb)
+    E = H.grouped_error_bound(qa, sa, off, qb, sb)
     g, u, Eg, Eu = C[:, :I], C[:, I:], E[:, :I], E[:, I:]
     h = oracle.silu(g) * u
     rel = (4 + 1.2 * np.abs(g)) * 2.0 ** -23 + 2.0 ** -24
@@ -185,3 +170,68 @@ def test_swiglu_quant_extreme_gates(cuda_lib):
     sel = exact & same
     assert sel.sum() > T * I // 4
     assert np.array_equal(q.cpu().numpy()[sel], q_o[sel])
+
+
+def _sampled_experts(counts):
+    """First, last, fullest, emptiest non-empty and median non-empty expert."""
+    nz = np.nonzero(counts)[0]
+    return sorted({int(nz[0]), int(nz[-1]), int(np.argmax(counts)), int(nz[np.argmin(counts[nz])]),
+                   int(nz[len(nz) // 2])})
+
+
+def test_full_routed_layer_fused_up_and_down(cuda_lib):
+    """The routed-expert layer at full size, as the benchmark runs it: 8192 tokens of width
+    7168, top-8 of 256 experts (page 5, inprokorea.com free #890463, MoE configuration
+    passage), the fused up-projection + SwiGLU + power-of-2 quantisation of h over all
+    experts, then the K = 2048 down-projection fed from that h.  Five experts are checked
+    against the oracle: h's codes where the rounding is decided, the down-projection
+    per element and normwise (both sides consume the GPU's h codes)."""
+    case = synth.MOE_FULL
+    tok = case.tokens()
+    r = synth.moe_route(H.f32(tok), case.router(), case.bias(), case.topk)
+    off, counts = r["offsets"], r["counts"]
+    E, Hd, I, T = case.E, case.H, case.I, case.rows
+    qx, sx = cuda_lib.act_quant(tok.cuda(), pow2=True)
+    idx = torch.from_numpy(r["token_of_row"]).cuda()
+    qa, sa = qx.index_select(0, idx).contiguous(), sx.index_select(0, idx).contiguous()
+    qu = torch.empty((E, 2 * I, Hd), dtype=torch.uint8, device="cuda")
+    su = torch.empty((E, 2 * I // 128, Hd // 128), dtype=torch.float32, device="cuda")
+    qd = torch.empty((E, Hd, I), dtype=torch.uint8, device="cuda")
+    sd = torch.empty((E, Hd // 128, I // 128), dtype=torch.float32, device="cuda")
+    for e in range(E):
+        q_e, s_e = cuda_lib.weight_quant(synth.expert_weight(case, e, "up", "cuda"))
+        qu[e].copy_(q_e)
+        su[e].copy_(s_e)
+        q_e, s_e = cuda_lib.weight_quant(synth.expert_weight(case, e, "down", "cuda"))
+        qd[e].copy_(q_e)
+        sd[e].copy_(s_e)
+    dev_off = H.to_dev(off)
+    raw_h, qh = H.guarded_empty((T, I), torch.uint8)
+    raw_s, sh = H.guarded_empty((T, I // 128), torch.float32)
+    cuda_lib.grouped_swiglu_quant(qa, sa, dev_off, qu, su, out=qh, out_scales=sh)
+    raw_d, down = H.guarded_empty((T, Hd), torch.bfloat16)
+    cuda_lib.grouped_gemm(qh, sh, dev_off, qd, sd, out=down)
+    assert cuda_lib.device_status() == cuda_lib.OK
+    assert H.guards_intact(raw_h) and H.guards_intact(raw_s) and H.guards_intact(raw_d)
+
+    qx_r, sx_r = H.oracle_act_quant_rows(H.f32(tok), pow2=True)
+    assert np.array_equal(qx.cpu().numpy(), qx_r)
+    qh_g, sh_g, down_g = qh.cpu().numpy(), sh.cpu().numpy(), down.cpu()
+    for e in _sampled_experts(counts):
+        rows = slice(int(off[e]), int(off[e + 1]))
+        n = rows.stop - rows.start
+        toks = r["token_of_row"][rows]
+        qa_e, sa_e = qx_r[toks], sx_r[toks]
+        qu_r, su_r = oracle.weight_quant(H.f32(synth.expert_weight(case, e, "up", "cuda").cpu()))
+        assert np.array_equal(qu[e].cpu().numpy(), qu_r) and np.array_equal(su[e].cpu().numpy(), su_r)
+        off_e = np.array([0, n], np.int32)
+        _, _, h_o = oracle.grouped_swiglu_quant(qa_e, sa_e, off_e, qu_r[None], su_r[None], pow2=True)
+        bound_h = _h_error_bound(qa_e, sa_e, off_e, qu_r[None], su_r[None])
+        decided = H.check_quant_decisions(qh_g[rows], sh_g[rows], h_o, bound_h, pow2=True)
+        assert decided > 0.99, (e, decided)
+        qd_r, sd_r = oracle.weight_quant(H.f32(synth.expert_weight(case, e, "down", "cuda").cpu()))
+        assert np.array_equal(qd[e].cpu().numpy(), qd_r) and np.array_equal(sd[e].cpu().numpy(), sd_r)
+        ref = oracle.gemm(qh_g[rows], sh_g[rows], qd_r, sd_r)
+        assert H.normwise_rel_err(down_g[rows], ref) <= 4e-3, e
+        H.assert_elementwise(down_g[rows], ref, H.gemm_error_bound(qh_g[rows], sh_g[rows], qd_r, sd_r),
+                             f"full routed down, expert {e} ({n} rows)")
