@@ -88,10 +88,25 @@ def _check(status: int, where: str) -> None:
         raise Fp8Error(status, where)
 
 
-def _stream(stream) -> int:
+def _stream(stream, device: torch.device) -> int:
+    """Raw handle of `stream` (default: the current stream of `device`)."""
     if stream is None:
-        stream = torch.cuda.current_stream()
+        stream = torch.cuda.current_stream(device)
+    elif stream.device != device:
+        raise ValueError(f"stream is on {stream.device}, the tensors on {device}")
     return int(stream.cuda_stream)
+
+
+def _same_device(*tensors) -> torch.device:
+    """The one CUDA device every given tensor lives on (None entries are skipped).
+
+    The library launches on the calling thread's current device and builds its
+    TMA descriptors over the raw pointers, so operands on another GPU would be
+    read as peer memory; mixed devices are rejected here instead."""
+    devs = {t.device for t in tensors if t is not None}
+    if len(devs) != 1:
+        raise ValueError(f"all tensors must be on one CUDA device, got {sorted(map(str, devs))}")
+    return devs.pop()
 
 
 def _ptr(t: torch.Tensor | None) -> int | None:
@@ -114,6 +129,13 @@ def _src_dtype(t: torch.Tensor) -> int:
 _SRC = (torch.bfloat16, torch.float32)
 
 
+def _run(fn: str, device: torch.device, *args) -> int:
+    """Call library entry point `fn` with `device` current (the library launches on
+    the calling thread's current device)."""
+    with torch.cuda.device(device):
+        return getattr(load(), fn)(*args)
+
+
 def act_quant(x: torch.Tensor, pow2: bool = False, transpose: bool = False, stream=None):
     """1x128 tiles -> (q uint8 [M, K], s float32 [M, K/128]);
     transpose=True: 128x1 tiles -> (q [K, M], s [K, M/128])."""
@@ -126,8 +148,9 @@ def act_quant(x: torch.Tensor, pow2: bool = False, transpose: bool = False, stre
         q = torch.empty((M, K), dtype=torch.uint8, device=x.device)
         s = torch.empty((M, K // 128 if K % 128 == 0 else 1), dtype=torch.float32, device=x.device)
     flags = (POW2 if pow2 else 0) | (TRANSPOSE if transpose else 0)
-    _check(load().fp8_act_quant(_ptr(x), _src_dtype(x), M, K, _ptr(q), _ptr(s), flags,
-                                _stream(stream)), "fp8_act_quant")
+    dev = x.device
+    _check(_run("fp8_act_quant", dev, _ptr(x), _src_dtype(x), M, K, _ptr(q), _ptr(s), flags,
+                _stream(stream, dev)), "fp8_act_quant")
     return q, s
 
 
@@ -141,9 +164,9 @@ def weight_quant(w: torch.Tensor, pow2: bool = False, transposed: bool = False, 
     if transposed:
         qt = torch.empty((K, N), dtype=torch.uint8, device=w.device)
         st = torch.empty((max(K // 128, 1), max(N // 128, 1)), dtype=torch.float32, device=w.device)
-    _check(load().fp8_weight_quant(_ptr(w), _src_dtype(w), N, K, _ptr(q), _ptr(s), _ptr(qt),
-                                   _ptr(st), POW2 if pow2 else 0, _stream(stream)),
-           "fp8_weight_quant")
+    dev = w.device
+    _check(_run("fp8_weight_quant", dev, _ptr(w), _src_dtype(w), N, K, _ptr(q), _ptr(s), _ptr(qt),
+                _ptr(st), POW2 if pow2 else 0, _stream(stream, dev)), "fp8_weight_quant")
     return (q, s, qt, st) if transposed else (q, s)
 
 
@@ -151,12 +174,12 @@ def requant_transpose(q: torch.Tensor, s: torch.Tensor, pow2: bool = False, stre
     """Stored 1x128 codes (q [M, K], s [M, K/128]) -> 128x1 tiles (q_t [K, M], s_t [K, M/128])."""
     _need(q, (torch.uint8,), "q")
     _need(s, (torch.float32,), "s")
+    dev = _same_device(q, s)
     M, K = q.shape
-    qt = torch.empty((K, M), dtype=torch.uint8, device=q.device)
-    st = torch.empty((K, M // 128 if M % 128 == 0 else 1), dtype=torch.float32, device=q.device)
-    _check(load().fp8_requant_transpose(_ptr(q), _ptr(s), M, K, _ptr(qt), _ptr(st),
-                                        POW2 if pow2 else 0, _stream(stream)),
-           "fp8_requant_transpose")
+    qt = torch.empty((K, M), dtype=torch.uint8, device=dev)
+    st = torch.empty((K, M // 128 if M % 128 == 0 else 1), dtype=torch.float32, device=dev)
+    _check(_run("fp8_requant_transpose", dev, _ptr(q), _ptr(s), M, K, _ptr(qt), _ptr(st),
+                POW2 if pow2 else 0, _stream(stream, dev)), "fp8_requant_transpose")
     return qt, st
 
 
@@ -178,17 +201,17 @@ def gemm(a, sa, b, sb, out_dtype=torch.bfloat16, b_tile: bool = False, out=None,
         _need(t, (torch.uint8,), n)
     for t, n in ((sa, "sa"), (sb, "sb")):
         _need(t, (torch.float32,), n)
+    dev = _same_device(a, sa, b, sb, out)
     M, K = a.shape
     N = b.shape[0]
     if b.shape[1] != K:
         raise ValueError("a and b disagree on K")
     if out is None:
-        out = torch.empty((M, N), dtype=out_dtype, device=a.device)
+        out = torch.empty((M, N), dtype=out_dtype, device=dev)
     _need(out, (torch.bfloat16, torch.float32), "out")
-    _check(load().fp8_blockscaled_gemm(_ptr(a), _ptr(sa), _ptr(b), _ptr(sb), _ptr(out),
-                                       _out_code(out.dtype), M, N, K,
-                                       (B_TILE1x128 if b_tile else 0) | (WHOLE_K if whole_k else 0),
-                                       _stream(stream)),
+    flags = (B_TILE1x128 if b_tile else 0) | (WHOLE_K if whole_k else 0)
+    _check(_run("fp8_blockscaled_gemm", dev, _ptr(a), _ptr(sa), _ptr(b), _ptr(sb), _ptr(out),
+                _out_code(out.dtype), M, N, K, flags, _stream(stream, dev)),
            "fp8_blockscaled_gemm")
     return out
 
@@ -200,19 +223,20 @@ def gemm_quant(a, sa, b, sb, b_tile: bool = False, pow2: bool = False, out=None,
         _need(t, (torch.uint8,), n)
     for t, n in ((sa, "sa"), (sb, "sb")):
         _need(t, (torch.float32,), n)
+    dev = _same_device(a, sa, b, sb, out, out_scales)
     M, K = a.shape
     N = b.shape[0]
     if b.shape[1] != K:
         raise ValueError("a and b disagree on K")
     if out is None:
-        out = torch.empty((M, N), dtype=torch.uint8, device=a.device)
+        out = torch.empty((M, N), dtype=torch.uint8, device=dev)
     if out_scales is None:
-        out_scales = torch.empty((M, max(N // 128, 1)), dtype=torch.float32, device=a.device)
+        out_scales = torch.empty((M, max(N // 128, 1)), dtype=torch.float32, device=dev)
     _need(out, (torch.uint8,), "out")
     _need(out_scales, (torch.float32,), "out_scales")
     flags = (B_TILE1x128 if b_tile else 0) | (POW2 if pow2 else 0)
-    _check(load().fp8_blockscaled_gemm_quant(_ptr(a), _ptr(sa), _ptr(b), _ptr(sb), _ptr(out),
-                                             _ptr(out_scales), M, N, K, flags, _stream(stream)),
+    _check(_run("fp8_blockscaled_gemm_quant", dev, _ptr(a), _ptr(sa), _ptr(b), _ptr(sb), _ptr(out),
+                _ptr(out_scales), M, N, K, flags, _stream(stream, dev)),
            "fp8_blockscaled_gemm_quant")
     return out, out_scales
 
@@ -224,15 +248,16 @@ def grouped_gemm(a, sa, offsets, b, sb, out_dtype=torch.bfloat16, out=None, stre
     _need(sa, (torch.float32,), "sa")
     _need(sb, (torch.float32,), "sb")
     _need(offsets, (torch.int32,), "offsets")
+    dev = _same_device(a, sa, offsets, b, sb, out)
     T, K = a.shape
     E, N, Kb = b.shape
     if Kb != K or offsets.numel() != E + 1:
         raise ValueError("shape mismatch between a, b and offsets")
     if out is None:
-        out = torch.empty((T, N), dtype=out_dtype, device=a.device)
+        out = torch.empty((T, N), dtype=out_dtype, device=dev)
     _need(out, (torch.bfloat16, torch.float32), "out")
-    _check(load().fp8_grouped_gemm(_ptr(a), _ptr(sa), _ptr(offsets), E, T, _ptr(b), _ptr(sb),
-                                   _ptr(out), _out_code(out.dtype), N, K, 0, _stream(stream)),
+    _check(_run("fp8_grouped_gemm", dev, _ptr(a), _ptr(sa), _ptr(offsets), E, T, _ptr(b), _ptr(sb),
+                _ptr(out), _out_code(out.dtype), N, K, 0, _stream(stream, dev)),
            "fp8_grouped_gemm")
     return out
 
@@ -247,35 +272,44 @@ def grouped_swiglu_quant(a, sa, offsets, b, sb, pow2: bool = True, out=None, out
     _need(sa, (torch.float32,), "sa")
     _need(sb, (torch.float32,), "sb")
     _need(offsets, (torch.int32,), "offsets")
+    dev = _same_device(a, sa, offsets, b, sb, out, out_scales)
     T, K = a.shape
     E, N, Kb = b.shape
     if Kb != K or offsets.numel() != E + 1:
         raise ValueError("shape mismatch between a, b and offsets")
     I = N // 2
     if out is None:
-        out = torch.empty((T, I), dtype=torch.uint8, device=a.device)
+        out = torch.empty((T, I), dtype=torch.uint8, device=dev)
     if out_scales is None:
-        out_scales = torch.empty((T, max(I // 128, 1)), dtype=torch.float32, device=a.device)
+        out_scales = torch.empty((T, max(I // 128, 1)), dtype=torch.float32, device=dev)
     _need(out, (torch.uint8,), "out")
     _need(out_scales, (torch.float32,), "out_scales")
-    _check(load().fp8_grouped_gemm_swiglu_quant(_ptr(a), _ptr(sa), _ptr(offsets), E, T, _ptr(b),
-                                                _ptr(sb), _ptr(out), _ptr(out_scales), N, K,
-                                                POW2 if pow2 else 0, _stream(stream)),
+    _check(_run("fp8_grouped_gemm_swiglu_quant", dev, _ptr(a), _ptr(sa), _ptr(offsets), E, T,
+                _ptr(b), _ptr(sb), _ptr(out), _ptr(out_scales), N, K, POW2 if pow2 else 0,
+                _stream(stream, dev)),
            "fp8_grouped_gemm_swiglu_quant")
     return out, out_scales
 
 
-def device_status(stream=None) -> int:
-    """Synchronise the stream; return and clear the library's device status word."""
-    return int(load().fp8_get_device_status(_stream(stream)))
+def _device_arg(device) -> torch.device:
+    return torch.device("cuda", torch.cuda.current_device()) if device is None else \
+        torch.device(device)
+
+
+def device_status(stream=None, device=None) -> int:
+    """Synchronise the stream; return and clear the library's device status word
+    of that stream's device (default: the current device)."""
+    dev = stream.device if stream is not None else _device_arg(device)
+    return int(_run("fp8_get_device_status", dev, _stream(stream, dev)))
 
 
 def set_wait_limit(cycles: int) -> None:
     load().fp8fg_set_wait_limit(int(cycles))
 
 
-def selftest_wait_timeout(limit_cycles: int = 1 << 20, stream=None) -> int:
+def selftest_wait_timeout(limit_cycles: int = 1 << 20, stream=None, device=None) -> int:
     """Run the bounded-wait self-test; returns the device status it produced."""
-    _check(load().fp8fg_selftest_wait_timeout(int(limit_cycles), _stream(stream)),
+    dev = stream.device if stream is not None else _device_arg(device)
+    _check(_run("fp8fg_selftest_wait_timeout", dev, int(limit_cycles), _stream(stream, dev)),
            "fp8fg_selftest_wait_timeout")
-    return device_status(stream)
+    return device_status(stream, dev)

@@ -21,17 +21,10 @@ __device__ int g_device_status = 0;
 
 namespace {
 
-constexpr int kMaxDevices = 64;
 constexpr int64_t kMaxDim = (int64_t{1} << 31) - 1;
 constexpr uint64_t kDefaultWaitLimit = uint64_t{1} << 32;  // ~2 s at 2 GHz
 
 std::atomic<uint64_t> g_wait_limit{0};
-
-int current_device() {
-  int d = -1;
-  if (cudaGetDevice(&d) != cudaSuccess || d < 0 || d >= kMaxDevices) return -1;
-  return d;
-}
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -49,6 +42,12 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 }
 
 }  // namespace
+
+int current_device() {
+  int d = -1;
+  if (cudaGetDevice(&d) != cudaSuccess || d < 0 || d >= kMaxDevices) return -1;
+  return d;
+}
 
 int device_sm_count() {
   static std::atomic<int> cache[kMaxDevices] = {};

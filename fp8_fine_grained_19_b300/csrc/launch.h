@@ -7,8 +7,15 @@
 
 #include "fp8fg.h"
 
+#include <atomic>
+
 namespace fp8fg {
 
+// Devices the per-device caches below can track (device indices 0 .. 63).
+constexpr int kMaxDevices = 64;
+
+// Index of the calling thread's current device, or -1 (no device, or >= kMaxDevices).
+int current_device();
 // Number of SMs of the current device (cached per device).
 int device_sm_count();
 // Cycle limit applied to every pipeline wait of the next launches.
@@ -45,6 +52,21 @@ fp8fg_status launch_grouped_swiglu_quant(const uint8_t* a, const float* sa,
                                          int64_t N, int64_t K, bool pow2, cudaStream_t st);
 // Failure-detection self-test: one wait that nothing completes.
 cudaError_t launch_wait_timeout_selftest(uint32_t limit_cycles, cudaStream_t st);
+
+// Raise kernel `Kernel`'s dynamic shared-memory limit to `bytes` on the current
+// device.  The attribute belongs to the device's context, so it is set once per
+// device (and again if a previous attempt failed), not once per process.
+template <auto Kernel>
+cudaError_t set_max_dynamic_smem(int bytes) {
+  static std::atomic<int> done[kMaxDevices] = {};
+  const int d = current_device();
+  if (d < 0) return cudaErrorInvalidDevice;
+  if (done[d].load(std::memory_order_acquire)) return cudaSuccess;
+  const cudaError_t e =
+      cudaFuncSetAttribute(Kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess) done[d].store(1, std::memory_order_release);
+  return e;
+}
 
 // Encode a tensor map (innermost dimension first, zero fill); returns false if
 // the driver rejects it.

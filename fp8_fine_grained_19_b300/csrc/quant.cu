@@ -571,15 +571,13 @@ cudaError_t launch_act_quant_cols(const void* x, fp8fg_dtype xt, int64_t M, int6
   const int grid = static_cast<int>(n_tiles < max_ctas ? n_tiles : max_ctas);
   const int smem = kColStages * 32768;
   if (bf16) {
-    static const cudaError_t attr = cudaFuncSetAttribute(
-        act_quant_cols_kernel<__nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    const cudaError_t attr = set_max_dynamic_smem<act_quant_cols_kernel<__nv_bfloat16>>(smem);
     if (attr != cudaSuccess) return attr;
     act_quant_cols_kernel<__nv_bfloat16><<<grid, kColThreads, smem, st>>>(
         map, qt, st_, static_cast<int>(M), static_cast<int>(K), pow2 ? 1 : 0, wait_limit_cycles(),
         device_status_word());
   } else {
-    static const cudaError_t attr = cudaFuncSetAttribute(
-        act_quant_cols_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    const cudaError_t attr = set_max_dynamic_smem<act_quant_cols_kernel<float>>(smem);
     if (attr != cudaSuccess) return attr;
     act_quant_cols_kernel<float><<<grid, kColThreads, smem, st>>>(
         map, qt, st_, static_cast<int>(M), static_cast<int>(K), pow2 ? 1 : 0, wait_limit_cycles(),
@@ -606,8 +604,7 @@ cudaError_t launch_weight_quant(const void* w, fp8fg_dtype wt, int64_t N, int64_
         static_cast<int>(K), pow2 ? 1 : 0);
   } else {
     constexpr int smem = 128 * 128 * 4;
-    static const cudaError_t attr = cudaFuncSetAttribute(
-        weight_quant_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    const cudaError_t attr = set_max_dynamic_smem<weight_quant_kernel<float>>(smem);
     if (attr != cudaSuccess) return attr;
     weight_quant_kernel<float><<<grid, 256, smem, st>>>(static_cast<const float*>(w), q, s, qt,
                                                         st_, static_cast<int>(N),

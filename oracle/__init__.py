@@ -1,9 +1,10 @@
 """CPU oracle for fine-grained FP8 quantisation and the block-scaled FP8 GEMM.
 
 TEST INFRASTRUCTURE ONLY.  Plain numpy, float64/int64 where precision matters,
-written from the DeepSeek-V3 FP8 training passages on the five scraped pages
-(cited per function as page + passage/figure; the page names are listed in
-the design notes).  It shares no code, header, table or constant generator
+written from the DeepSeek-V3 FP8 training passages on the five scraped pages,
+cited per function as page + passage/figure: page 1 = xn--9g3bo1gtkw0l8ubf92bgle.kr
+qna #85187, page 2 = inprokorea.com free #735329, page 5 = inprokorea.com free
+#890463 (pages 3 and 4 hold nothing on this path).  It shares no code, header, table or constant generator
 with the CUDA library, and the CUDA library never imports it.  Only the tests,
 the smoke check and the benchmark's CPU-baseline leg may call it.
 

@@ -13,11 +13,19 @@ Sources (page, passage):
   * backward re-quantisation into 128x1 tiles -- page 5 (inprokorea.com free
     #890463), passage on the backward pass.
 
-Readings where the pages are silent (listed in the design notes):
-  amax' = max(amax, 2^-64); dequant scale s = fl32(amax'/448); the codes are
-  encode(fl32(x * fl32(448/amax'))) -- one rounded multiply, not x/s.
-  Power-of-2 mode: s = 2^ceil(log2(fl32(amax'/448))) and the multiplier is 1/s
-  (exact).  The stored scale is always the dequantisation scale: x ~ decode(q)*s.
+Readings where the pages are silent (the pages give the tile shapes, the
+online amax and the FP32 scale storage, but no formula):
+  * amax' = max(amax, 2^-64): an all-zero or tiny tile still gets a finite,
+    nonzero scale (the floor never binds on the workloads' data);
+  * the stored scale is the dequantisation scale, s = fl32(amax'/448), so the
+    tile amax maps to exactly +-448 (E4M3's largest finite value) and
+    x ~ decode(q) * s, the direction in which page 2 multiplies it in;
+  * the codes are encode(fl32(x * fl32(448/amax'))): one rounded multiply per
+    element, not a division x/s;
+  * power-of-2 mode rounds up, s = 2^ceil(log2(fl32(amax'/448))), so no scaled
+    value exceeds 448; its multiplier 1/s is exact;
+  * E4M3 rounding is to nearest even, saturating to +-448, keeping the sign of
+    zero (e4m3.encode).
 """
 
 from __future__ import annotations

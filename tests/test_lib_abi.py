@@ -152,3 +152,14 @@ def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(fp8, "lib_path", lambda: str(tmp_path / "missing.so"))
     with pytest.raises(RuntimeError):
         fp8.load()
+
+
+def test_binding_rejects_mixed_devices():
+    # the library launches on the current device and reads raw pointers, so a
+    # call whose tensors live on different devices must not reach it
+    import torch
+    a = torch.empty(4)
+    b = torch.empty(4, device="meta")
+    with pytest.raises(ValueError):
+        fp8._same_device(a, b)
+    assert fp8._same_device(a, None, a) == a.device
