@@ -40,8 +40,10 @@
 // boxes so that a thread holds g and u of the same 64 outputs, forms
 // h = silu(g) * u and stores h's codes and power-of-2 scales; EPI_WHOLEK is a
 // study mode that accumulates all of K in TMEM with per-tensor scales.
-// Tiles are visited in groups of 16 M-tiles (all N-tiles of a group before the
-// next), so a group's A rows stay in L2 while B streams once per group.
+// Tiles are visited in groups of M-tiles (all N-tiles of a group before the
+// next), so a group's A rows stay in L2 while B streams once per group.  The
+// host sizes a group to at most kGroupABytes of A (the Fprop shape, M = 4096 at
+// K = 7168, is one group: B is read from DRAM once).
 // Every pipeline wait is bounded (FP8FG_ERR_TIMEOUT, see device_common.cuh).
 
 #include <cuda_bf16.h>
@@ -84,7 +86,9 @@ __host__ __device__ constexpr int regs_producer(bool grouped, int epi) {
 static_assert(2 * SWIGLU_REGS_EPILOGUE + regs_producer(true, 2) <= 3 * REGS_LAUNCH, "register split");
 static_assert(2 * GROUPED_REGS_EPILOGUE + regs_producer(true, 0) <= 3 * REGS_LAUNCH, "register split");
 constexpr int TMEM_COLS = 512;
-constexpr int GROUP_M = 16;
+// A bytes one tile group may hold in L2 (126 MB): room is left for the B tiles
+// in flight and the output's write-back.
+constexpr int64_t kGroupABytes = int64_t{48} << 20;
 constexpr int MAX_EXPERTS = 1024;
 constexpr int SB_GROUP = 8;           // tile mode: slices whose B scales are shared per barrier
 constexpr int CST_BYTES = 2048;       // output staging per promotion warp: 32 rows x 64 bytes
@@ -107,6 +111,7 @@ struct GemmParams {
   int M;                  // dense: rows of A/C; grouped: total rows
   int N, K, nkb;
   int m_tiles, n_tiles;   // dense tiling (m_tiles unused when grouped)
+  int group_m;            // dense: M-tiles per tile group (see tile_of)
   int E;
   int c_f32;
   int b_tile;
@@ -159,10 +164,10 @@ template <bool GROUPED>
 __device__ __forceinline__ Tile tile_of(int t, const GemmParams& p, const Smem& sm) {
   Tile r;
   if constexpr (!GROUPED) {
-    const int group = GROUP_M * p.n_tiles;
+    const int group = p.group_m * p.n_tiles;
     const int g = t / group;
-    const int first = g * GROUP_M;
-    const int gm = min(GROUP_M, p.m_tiles - first);
+    const int first = g * p.group_m;
+    const int gm = min(p.group_m, p.m_tiles - first);
     const int local = t - g * group;
     const int mb = first + local % gm;
     const int nb = local / gm;
@@ -856,12 +861,19 @@ bool make_c_map(CUtensorMap* mC, void* c, fp8fg_dtype ct, int64_t rows, int64_t 
                            c, 2, dC, sC, boxC, CU_TENSOR_MAP_SWIZZLE_64B);
 }
 
+// M-tiles per tile group of a dense launch: as many as keep the group's A rows
+// within kGroupABytes, at least 8, at most all of them.
+int group_m_tiles(int64_t m_tiles, int64_t K) {
+  int64_t g = kGroupABytes / (static_cast<int64_t>(BM) * K);
+  if (g < 8) g = 8;
+  if (g > m_tiles) g = m_tiles;
+  return static_cast<int>(g < 1 ? 1 : g);
+}
+
 template <bool GROUPED, bool BTILE, int EPI = EPI_STORE>
 cudaError_t set_smem_attr() {
-  static const cudaError_t e = cudaFuncSetAttribute(
-      blockscaled_gemm_kernel<GROUPED, BTILE, EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  return set_max_dynamic_smem<blockscaled_gemm_kernel<GROUPED, BTILE, EPI>>(
       static_cast<int>(kSmemBytes));
-  return e;
 }
 
 }  // namespace
@@ -887,6 +899,7 @@ fp8fg_status launch_gemm(const uint8_t* a, const float* sa, const uint8_t* b, co
   p.nkb = static_cast<int>(K / BK);
   p.m_tiles = static_cast<int>((M + BM - 1) / BM);
   p.n_tiles = static_cast<int>((N + BN - 1) / BN);
+  p.group_m = group_m_tiles(p.m_tiles, K);
   p.E = 1;
   p.c_f32 = ct == FP8FG_F32;
   p.b_tile = b_tile ? 1 : 0;
@@ -930,6 +943,7 @@ fp8fg_status launch_gemm_quant(const uint8_t* a, const float* sa, const uint8_t*
   p.nkb = static_cast<int>(K / BK);
   p.m_tiles = static_cast<int>((M + BM - 1) / BM);
   p.n_tiles = static_cast<int>((N + BN - 1) / BN);
+  p.group_m = group_m_tiles(p.m_tiles, K);
   p.E = 1;
   p.c_f32 = 0;
   p.b_tile = b_tile ? 1 : 0;
