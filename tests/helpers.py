@@ -147,13 +147,15 @@ def gemm_error_bound(qa, sa, qb, sb, b_tile=False) -> np.ndarray:
     into an FP32 accumulator with one rounding per group (page 2,
     inprokorea.com free #735329, promotion passage and Figure 6).  With
     A1 = sum_kb |P_kb| s_kb and A2 = sum_kb s_kb sum_{k in kb} |a_k b_k|:
-      * group partials: |T_kb - P_kb| <= 16 * 2^-24 * sum_{k in kb} |a_k b_k|
-        (four accumulation steps, each allowed 4 units of 2^-24 of the group's
-        magnitude sum; B300 measured at 25-26 bits of accumulation);
+      * group partials: |T_kb - P_kb| <= 8 * 2^-24 * sum_{k in kb} |a_k b_k|
+        (four K=32 accumulation steps; B300's FP8 accumulation measured like an
+        aligned sum truncated to 25-26 significant bits, so each step loses at
+        most 2^-23 of the magnitude it aligns to, itself at most the group's
+        sum of |products|);
       * the scale product: 2^-24 |P_kb s_kb|;
       * the FP32 accumulation: at most nkb roundings of 2^-24 of a running sum
         bounded by A1.
-    Hence |C32 - C| <= (nkb + 1) 2^-24 A1 + 16 * 2^-24 A2 (second-order terms are
+    Hence |C32 - C| <= (nkb + 1) 2^-24 A1 + 8 * 2^-24 A2 (second-order terms are
     far below the first-order slack).  A single wrong element (a dropped group, a
     wrong scale) misses it by orders of magnitude.
     """
@@ -175,7 +177,7 @@ def gemm_error_bound(qa, sa, qb, sb, b_tile=False) -> np.ndarray:
         s = sa64[:, kb][:, None] * sbk[None, :]
         A1 += np.abs(P) * s
         A2 += Q * s
-    return (nkb + 1) * 2.0 ** -24 * A1 + 16 * 2.0 ** -24 * A2
+    return (nkb + 1) * 2.0 ** -24 * A1 + 8 * 2.0 ** -24 * A2
 
 
 def grouped_error_bound(qa, sa, offsets, qb, sb) -> np.ndarray:
