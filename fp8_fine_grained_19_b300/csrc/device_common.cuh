@@ -255,6 +255,25 @@ __device__ __forceinline__ uint64_t mul2(uint64_t a, uint64_t b) {
   asm volatile("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
   return d;
 }
+// The same two operations as fma2 / mul2, issued as two scalar IEEE
+// instructions on the pair's halves (identical results).  The tile-scale
+// promotion, which does a multiply and an FMA per element, measured 10-15 %
+// faster this way; the block-scale promotion is faster with the packed forms.
+__device__ __forceinline__ void fma2_s(uint64_t& acc, uint64_t a, uint64_t b) {
+  asm("{\n .reg .f32 c0, c1, a0, a1, b0, b1;\n mov.b64 {c0, c1}, %0;\n mov.b64 {a0, a1}, %1;\n"
+      " mov.b64 {b0, b1}, %2;\n fma.rn.f32 c0, a0, b0, c0;\n fma.rn.f32 c1, a1, b1, c1;\n"
+      " mov.b64 %0, {c0, c1};\n}\n"
+      : "+l"(acc)
+      : "l"(a), "l"(b));
+}
+__device__ __forceinline__ uint64_t mul2_s(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("{\n .reg .f32 d0, d1, a0, a1, b0, b1;\n mov.b64 {a0, a1}, %1;\n mov.b64 {b0, b1}, %2;\n"
+      " mul.rn.f32 d0, a0, b0;\n mul.rn.f32 d1, a1, b1;\n mov.b64 %0, {d0, d1};\n}\n"
+      : "=l"(d)
+      : "l"(a), "l"(b));
+  return d;
+}
 
 // ------------------------------------------------------- E4M3 tile scales
 // Scale rule of every 1x128 tile / 128x128 block (page 2, inprokorea.com free

@@ -90,7 +90,9 @@ constexpr int TMEM_COLS = 512;
 // in flight and the output's write-back.
 constexpr int64_t kGroupABytes = int64_t{48} << 20;
 constexpr int MAX_EXPERTS = 1024;
-constexpr int SB_GROUP = 8;           // tile mode: slices whose B scales are shared per barrier
+constexpr int SCALE_WARP = 10;        // tile mode: loads and transposes the B column scales
+constexpr int SB = 4;                 // tile mode: slices per scale-ring slot
+constexpr int SB_SLOTS = 3;           // tile mode: scale-ring slots
 constexpr int CST_BYTES = 2048;       // output staging per promotion warp: 32 rows x 64 bytes
 constexpr int CST_ROW = 64;           // bytes per staged row (the tensor map's 64-byte swizzle)
 constexpr uint32_t IDESC = idesc_e4m3_f32(BM, BN);
@@ -121,37 +123,48 @@ struct GemmParams {
   int* status;            // library status word
 };
 
-struct Smem {
+// Shared memory of one CTA.  The expert tables exist only in the grouped
+// kernels and the column-scale ring only in tile mode (BTILE), so that each
+// variant stays within the 227 KB a CTA may use.
+template <bool GROUPED, bool BTILE>
+struct SmemT {
   uint8_t a[STAGES][A_BYTES];     // 1024-byte aligned (offset 0)
   uint8_t b[STAGES][B_BYTES];
-  // Tile-mode B scales ([column half][group parity][slice][col], read as
-  // float4) during a tile's K loop; output staging of the promotion warps
-  // after it.  Warp w stages in bytes [2 KB w, 2 KB (w+1)), inside the scale
-  // ring of its own column half, and the half synchronises before the ring
-  // is rewritten.
-  union alignas(1024) {
-    float sbt[2][2][SB_GROUP][128];
-    uint8_t cst[NUM_EPI_WARPS][CST_BYTES];
-  };
+  // output staging of the promotion warps: warp w stages in bytes [2 KB w, 2 KB (w+1))
+  alignas(1024) uint8_t cst[NUM_EPI_WARPS][CST_BYTES];
+  // tile mode: the B column scales of SB slices of the current tile, [slice][column]
+  float sring[BTILE ? SB_SLOTS : 1][BTILE ? SB : 1][BTILE ? BN : 1];
   uint64_t full_bar[STAGES];
   uint64_t empty_bar[STAGES];
   uint64_t tfull_bar[2];
   uint64_t tempty_bar[2];
+  uint64_t sfull_bar[SB_SLOTS];   // tile mode: ring slot written by the scale warp
+  uint64_t sempty_bar[SB_SLOTS];  // tile mode: ring slot read by all promotion warps
   uint64_t drain_bar;
   uint32_t tmem_base;
   int abort_flag;
   int bad_offsets;
   int num_tiles;
   float amx[2][4][32];            // SwiGLU: per-row tile amax of each half (warp pairs)
-  int cum[MAX_EXPERTS + 1];       // grouped: tile prefix per expert
-  int row0[MAX_EXPERTS + 1];      // grouped: copy of offsets
+  int cum[GROUPED ? MAX_EXPERTS + 1 : 1];    // grouped: tile prefix per expert
+  int row0[GROUPED ? MAX_EXPERTS + 1 : 1];   // grouped: copy of offsets
 };
 
-static_assert(sizeof(Smem::sbt) == sizeof(Smem::cst), "staging spans the scale ring");
-static_assert(sizeof(Smem::sbt) / 2 == 4 * CST_BYTES, "a half's staging lies in its own ring");
-static_assert(offsetof(Smem, cst) % 1024 == 0, "swizzled TMA staging is 1024-byte aligned");
+using SmemDense = SmemT<false, false>;
+using SmemGrouped = SmemT<true, false>;
+using SmemTile = SmemT<false, true>;
+static_assert(offsetof(SmemDense, cst) % 1024 == 0, "swizzled TMA staging is 1024-byte aligned");
+static_assert(offsetof(SmemGrouped, cst) % 1024 == 0, "swizzled TMA staging is 1024-byte aligned");
+static_assert(offsetof(SmemTile, cst) % 1024 == 0, "swizzled TMA staging is 1024-byte aligned");
 static_assert(CST_BYTES == 32 * CST_ROW, "one staged chunk: 32 rows");
-static_assert(offsetof(Smem, full_bar) % 8 == 0, "mbarriers are 8-byte aligned");
+static_assert(offsetof(SmemTile, full_bar) % 8 == 0, "mbarriers are 8-byte aligned");
+static_assert(offsetof(SmemGrouped, full_bar) % 8 == 0, "mbarriers are 8-byte aligned");
+static_assert(offsetof(SmemTile, sring) % 16 == 0, "scale ring read as 16-byte pairs");
+template <bool GROUPED, bool BTILE>
+constexpr size_t smem_bytes() { return sizeof(SmemT<GROUPED, BTILE>) + 1024; }
+static_assert(smem_bytes<false, true>() <= 232448 && smem_bytes<true, false>() <= 232448 &&
+                  smem_bytes<false, false>() <= 232448,
+              "a CTA may use at most 227 KB of shared memory");
 
 struct Tile {
   int m0;       // first row of A / C
@@ -160,8 +173,8 @@ struct Tile {
   int e;        // expert (0 when dense)
 };
 
-template <bool GROUPED>
-__device__ __forceinline__ Tile tile_of(int t, const GemmParams& p, const Smem& sm) {
+template <bool GROUPED, class S>
+__device__ __forceinline__ Tile tile_of(int t, const GemmParams& p, const S& sm) {
   Tile r;
   if constexpr (!GROUPED) {
     const int group = p.group_m * p.n_tiles;
@@ -203,6 +216,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                             const __grid_constant__ CUtensorMap tmC, const GemmParams p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   // 1024-byte alignment of the operand stages (required by the 128B swizzle)
+  using Smem = SmemT<GROUPED, BTILE>;
   Smem& sm = *reinterpret_cast<Smem*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
 
@@ -219,6 +233,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     for (int b = 0; b < 2; ++b) {
       mbar_init(smem_u32(&sm.tfull_bar[b]), 1);
       mbar_init(smem_u32(&sm.tempty_bar[b]), NUM_EPI_WARPS);
+    }
+    for (int b = 0; b < SB_SLOTS; ++b) {
+      mbar_init(smem_u32(&sm.sfull_bar[b]), 1);
+      mbar_init(smem_u32(&sm.sempty_bar[b]), NUM_EPI_WARPS);
     }
     mbar_init(smem_u32(&sm.drain_bar), 1);
     fence_mbar_init();
@@ -367,17 +385,46 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         volatile int never = 0;
         mbar_wait(smem_u32(&sm.drain_bar), 0, p.wait_limit, &never, p.status);
       }
+    } else if (BTILE && warp == SCALE_WARP) {
+      // ----------------------------------------------- tile-mode scale loader
+      // For every SB slices of a tile, the 256 column scales sb[n0 + c, kb]
+      // (c = lane + 32 i) are read and written transposed, [slice][column],
+      // into a ring slot that the promotion warps read as 16-byte column
+      // pairs.  Columns past N read the last column's scales (never stored).
+      uint32_t grp = 0;
+      bool live = true;
+      for (int t = blockIdx.x; t < num_tiles && live; t += gridDim.x) {
+        const Tile tl = tile_of<GROUPED>(t, p, sm);
+        for (int kb0 = 0; kb0 < nkb; kb0 += SB, ++grp) {
+          const uint32_t slot = grp % SB_SLOTS;
+          if (!mbar_wait(smem_u32(&sm.sempty_bar[slot]), ((grp / SB_SLOTS) & 1) ^ 1, p.wait_limit,
+                         abort_flag, p.status)) {
+            live = false;
+            break;
+          }
+#pragma unroll
+          for (int i = 0; i < BN / 32; ++i) {
+            const int c = lane + 32 * i;
+            const float* col = p.sb + static_cast<int64_t>(min(tl.n0 + c, p.N - 1)) * nkb;
+#pragma unroll
+            for (int q = 0; q < SB; ++q)
+              sm.sring[slot][q][c] = kb0 + q < nkb ? __ldg(col + kb0 + q) : 0.0f;
+          }
+          __syncwarp();
+          if (lane == 0) mbar_arrive(smem_u32(&sm.sfull_bar[slot]));
+        }
+      }
     }
   } else {
     // ------------------------------------------------ promotion + epilogue
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(regs_epilogue(GROUPED, EPI)));
     const int quad = warp & 3;                      // TMEM lane quadrant
     const int half = warp >> 2;                     // N half of the tile
-    const int tid_h = threadIdx.x & 127;            // index within the half's warpgroup
     const int n_blocks = p.N / 128;                 // block-mode scale rows per expert
     const uint32_t lane_taddr = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + half * 128;
     uint32_t it = 0;
     uint32_t tcount = 0;                            // tile counter (study mode buffers)
+    uint32_t sgrp = 0;                              // tile mode: scale-ring group counter
     bool staged = false;                            // a store of this warp may still read cst
     bool ok = true;
     for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
@@ -400,44 +447,29 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       for (int j = 0; j < 64; ++j) acc[j] = 0;
 
       if constexpr (BTILE) {
-        // Column scales: thread tid_h owns column col_h + tid_h of its half and
-        // reads that column's scales SB_GROUP slices at a time (contiguous in
-        // sb).  The half shares them through a two-group ring in shared memory
-        // and synchronises once per group.  A thread whose wait gives up keeps
-        // walking the slices (without touching TMEM) so that every thread of
-        // the half passes the same barriers; the half then leaves together.
-        const float* sb_col = p.sb + static_cast<int64_t>(min(col_h + tid_h, p.N - 1)) * nkb;
-        float grp[SB_GROUP];
-#pragma unroll
-        for (int i = 0; i < SB_GROUP; ++i) grp[i] = i < nkb ? __ldg(sb_col + i) : 0.0f;
-#pragma unroll
-        for (int i = 0; i < SB_GROUP; ++i) sm.sbt[half][0][i][tid_h] = grp[i];
-#pragma unroll
-        for (int i = 0; i < SB_GROUP; ++i)
-          grp[i] = SB_GROUP + i < nkb ? __ldg(sb_col + SB_GROUP + i) : 0.0f;
-        bar_sync(1 + half, 128);
-        bool dead = false;
+        // Column scales come from the scale warp's ring: each slot holds SB
+        // slices of this tile's 256 columns; a warp waits for a slot before
+        // its first slice and frees it after its last, so no barrier joins
+        // the promotion warps.
         float sa_next = __ldg(sa_row);
         for (int kb = 0; kb < nkb; ++kb, ++it) {
-          if (kb > 0 && kb % SB_GROUP == 0) {
-            const int g = kb / SB_GROUP;
-#pragma unroll
-            for (int i = 0; i < SB_GROUP; ++i) sm.sbt[half][g & 1][i][tid_h] = grp[i];
-#pragma unroll
-            for (int i = 0; i < SB_GROUP; ++i)
-              grp[i] = kb + SB_GROUP + i < nkb ? __ldg(sb_col + kb + SB_GROUP + i) : 0.0f;
-            bar_sync(1 + half, 128);
+          const uint32_t slot = sgrp % SB_SLOTS;
+          if (kb % SB == 0 && !mbar_wait(smem_u32(&sm.sfull_bar[slot]), (sgrp / SB_SLOTS) & 1,
+                                         p.wait_limit, abort_flag, p.status)) {
+            ok = false;
+            break;
           }
           const float sa_cur = sa_next;
           if (kb + 1 < nkb) sa_next = __ldg(sa_row + kb + 1);
           const uint32_t buf = it & 1, bpar = (it >> 1) & 1;
-          if (!dead)
-            dead = !mbar_wait(smem_u32(&sm.tfull_bar[buf]), bpar, p.wait_limit, abort_flag, p.status);
-          if (dead) continue;
+          if (!mbar_wait(smem_u32(&sm.tfull_bar[buf]), bpar, p.wait_limit, abort_flag, p.status)) {
+            ok = false;
+            break;
+          }
           tc_fence_after();
           const uint32_t taddr = lane_taddr + buf * BN;
           const uint64_t sa2 = pack2(__float_as_uint(sa_cur), __float_as_uint(sa_cur));
-          const uint32_t sbv = smem_u32(&sm.sbt[half][(kb / SB_GROUP) & 1][kb % SB_GROUP][0]);
+          const uint32_t sbv = smem_u32(&sm.sring[slot][kb % SB][half * 128]);
 #pragma unroll
           for (int c = 0; c < 4; ++c) {
             // the coefficients sa * sb[col] of this chunk are formed while its
@@ -449,21 +481,23 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             for (int j = 0; j < 8; ++j) {
               uint64_t q0, q1;
               lds_2x64(sbv + (c * 32 + 4 * j) * 4, q0, q1);
-              cf[2 * j] = mul2(q0, sa2);
-              cf[2 * j + 1] = mul2(q1, sa2);
+              cf[2 * j] = mul2_s(q0, sa2);
+              cf[2 * j + 1] = mul2_s(q1, sa2);
             }
             tmem_ld_wait();
 #pragma unroll
-            for (int j = 0; j < 16; ++j) fma2(acc[c * 16 + j], pack2(r[2 * j], r[2 * j + 1]), cf[j]);
+            for (int j = 0; j < 16; ++j) fma2_s(acc[c * 16 + j], pack2(r[2 * j], r[2 * j + 1]), cf[j]);
           }
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(smem_u32(&sm.tempty_bar[buf]));
+          if (kb % SB == SB - 1 || kb == nkb - 1) {
+            // this warp's reads of the slot are complete (their values were used above)
+            if (lane == 0) mbar_arrive(smem_u32(&sm.sempty_bar[slot]));
+            ++sgrp;
+          }
         }
-        if (bar_any(1 + half, 128, dead)) {
-          ok = false;
-          break;
-        }
+        if (!ok) break;
       } else if constexpr (EPI == EPI_WHOLEK) {
         // the whole K sum of this tile sits in buffer tcount % 2: scale it once
         const float s = __ldg(p.sa) * __ldg(p.sb);
@@ -794,12 +828,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           }
         }
       }
-      if constexpr (BTILE) {
-        // the next tile's scale ring overwrites this half's staging
-        if (lane == 0) bulk_wait_read_all();
-        __syncwarp();
-        bar_sync(1 + half, 128);
-      }
     }
     // the CTA's shared memory must outlive the reads of the last stores
     if (lane == 0) bulk_wait_all();
@@ -828,7 +856,6 @@ __global__ void wait_timeout_selftest_kernel(long long limit, int* status) {
   __syncthreads();
 }
 
-constexpr size_t kSmemBytes = sizeof(Smem) + 1024;
 
 bool make_maps(CUtensorMap* mA, CUtensorMap* mB, const uint8_t* a, int64_t rowsA,
                const uint8_t* b, int64_t E, int64_t N, int64_t K, uint32_t b_box_rows = BN) {
@@ -873,7 +900,7 @@ int group_m_tiles(int64_t m_tiles, int64_t K) {
 template <bool GROUPED, bool BTILE, int EPI = EPI_STORE>
 cudaError_t set_smem_attr() {
   return set_max_dynamic_smem<blockscaled_gemm_kernel<GROUPED, BTILE, EPI>>(
-      static_cast<int>(kSmemBytes));
+      static_cast<int>(smem_bytes<GROUPED, BTILE>()));
 }
 
 }  // namespace
@@ -908,12 +935,12 @@ fp8fg_status launch_gemm(const uint8_t* a, const float* sa, const uint8_t* b, co
   const int tiles = p.m_tiles * p.n_tiles;
   const int grid = tiles < device_sm_count() ? tiles : device_sm_count();
   if (b_tile)
-    blockscaled_gemm_kernel<false, true, EPI_STORE><<<grid, NUM_THREADS, kSmemBytes, st>>>(mA, mB, mC, p);
+    blockscaled_gemm_kernel<false, true, EPI_STORE><<<grid, NUM_THREADS, smem_bytes<false, true>(), st>>>(mA, mB, mC, p);
   else if (whole_k)
-    blockscaled_gemm_kernel<false, false, EPI_WHOLEK><<<grid, NUM_THREADS, kSmemBytes, st>>>(mA, mB, mC,
+    blockscaled_gemm_kernel<false, false, EPI_WHOLEK><<<grid, NUM_THREADS, smem_bytes<false, false>(), st>>>(mA, mB, mC,
                                                                                            p);
   else
-    blockscaled_gemm_kernel<false, false, EPI_STORE><<<grid, NUM_THREADS, kSmemBytes, st>>>(mA, mB, mC, p);
+    blockscaled_gemm_kernel<false, false, EPI_STORE><<<grid, NUM_THREADS, smem_bytes<false, false>(), st>>>(mA, mB, mC, p);
   return cudaGetLastError() == cudaSuccess ? FP8FG_OK : FP8FG_ERR_CUDA;
 }
 
@@ -954,9 +981,9 @@ fp8fg_status launch_gemm_quant(const uint8_t* a, const float* sa, const uint8_t*
   const int tiles = p.m_tiles * p.n_tiles;
   const int grid = tiles < device_sm_count() ? tiles : device_sm_count();
   if (b_tile)
-    blockscaled_gemm_kernel<false, true, EPI_QUANT><<<grid, NUM_THREADS, kSmemBytes, st>>>(mA, mB, mQ, p);
+    blockscaled_gemm_kernel<false, true, EPI_QUANT><<<grid, NUM_THREADS, smem_bytes<false, true>(), st>>>(mA, mB, mQ, p);
   else
-    blockscaled_gemm_kernel<false, false, EPI_QUANT><<<grid, NUM_THREADS, kSmemBytes, st>>>(mA, mB, mQ, p);
+    blockscaled_gemm_kernel<false, false, EPI_QUANT><<<grid, NUM_THREADS, smem_bytes<false, false>(), st>>>(mA, mB, mQ, p);
   return cudaGetLastError() == cudaSuccess ? FP8FG_OK : FP8FG_ERR_CUDA;
 }
 
@@ -985,7 +1012,7 @@ fp8fg_status launch_grouped_gemm(const uint8_t* a, const float* sa, const int32_
   p.b_tile = 0;
   p.wait_limit = wait_limit_cycles();
   p.status = device_status_word();
-  blockscaled_gemm_kernel<true, false, EPI_STORE><<<device_sm_count(), NUM_THREADS, kSmemBytes, st>>>(
+  blockscaled_gemm_kernel<true, false, EPI_STORE><<<device_sm_count(), NUM_THREADS, smem_bytes<true, false>(), st>>>(
       mA, mB, mC, p);
   return cudaGetLastError() == cudaSuccess ? FP8FG_OK : FP8FG_ERR_CUDA;
 }
@@ -1026,7 +1053,7 @@ fp8fg_status launch_grouped_swiglu_quant(const uint8_t* a, const float* sa,
   if (!encode_tensor_map(&mQ, CU_TENSOR_MAP_DATA_TYPE_UINT8, q, 2, dQ, sQ, boxQ,
                          CU_TENSOR_MAP_SWIZZLE_64B))
     return FP8FG_ERR_CUDA;
-  blockscaled_gemm_kernel<true, false, EPI_SWIGLU><<<device_sm_count(), NUM_THREADS, kSmemBytes,
+  blockscaled_gemm_kernel<true, false, EPI_SWIGLU><<<device_sm_count(), NUM_THREADS, smem_bytes<true, false>(),
                                                      st>>>(mA, mB, mQ, p);
   return cudaGetLastError() == cudaSuccess ? FP8FG_OK : FP8FG_ERR_CUDA;
 }
