@@ -424,12 +424,35 @@ def job_rate(world: int, units_per_rank: float, ms: float) -> float:
 
 def _timed_loop(ops, steps, warmup, stream, dev, world=1):
     """Run `ops` (list of (name, fn)) back to back `steps` times after `warmup`
-    untimed steps; CUDA events around the whole region and around every op."""
+    untimed steps; CUDA events around the whole region and around every op.
+
+    Each op is captured once into its own CUDA graph and replayed, and the
+    timed region is enqueued behind a GPU-side wait, so the host is ahead of
+    the GPU: the event times are the kernels', not the host's launch overhead
+    (which otherwise dominates ops of 5-30 us)."""
     import torch
 
+    # an op's fn may be a list: copies of the op on rotating input buffers, step i
+    # replays copy i % len (keeps the working set of consecutive steps above L2)
+    ops = [(name, fn if isinstance(fn, list) else [fn]) for name, fn in ops]
     for _ in range(max(warmup, 3)):
-        for _, fn in ops:
-            fn()
+        for _, fns in ops:
+            for fn in fns:
+                fn()
+    torch.cuda.synchronize()
+    graphs = []
+    for _, fns in ops:
+        gl = []
+        for fn in fns:
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                fn()
+            gl.append(g)
+        graphs.append(gl)
+    torch.cuda.synchronize()
+    for gl in graphs:                # one untimed replay of each
+        for g in gl:
+            g.replay()
     torch.cuda.synchronize()
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(ops) + 1)]
            for _ in range(steps)]
@@ -437,12 +460,13 @@ def _timed_loop(ops, steps, warmup, stream, dev, world=1):
     barrier(world)
     torch.cuda.synchronize()
     with ClockSampler(dev.index) as clk:
+        torch.cuda._sleep(100_000_000)   # ~50 ms on the GPU while the host enqueues ahead
         clk.mark("start")
         t0.record(stream)
         for i in range(steps):
-            for j, (_, fn) in enumerate(ops):
+            for j, gl in enumerate(graphs):
                 evs[i][j].record(stream)
-                fn()
+                gl[i % len(gl)].replay()
             evs[i][len(ops)].record(stream)
         t1.record(stream)
         torch.cuda.synchronize()
@@ -465,7 +489,12 @@ def run_workload(args, rank, world):
     torch.cuda.set_device(dev)
     lib = fp8.load()
     stream = torch.cuda.current_stream()
-    sp = stream.cuda_stream
+
+    def cur():
+        # the stream current at call time: the timed loop replays each op from a
+        # CUDA graph, which captures on its own stream
+        return torch.cuda.current_stream().cuda_stream
+
     pk = peaks()
     hbm = pk["hbm_gbs"]
 
@@ -496,30 +525,30 @@ def run_workload(args, rank, world):
         dx = torch.empty((Mt, Kh), dtype=torch.bfloat16, device=dev)
         # X as the forward pass stored it: E4M3 codes with 1x128 scales
         qx, sx = u8(Mt, Kh), f32(Mt, Kh // 128)
-        check(lib.fp8_act_quant(x.data_ptr(), fp8.BF16, Mt, Kh, qx.data_ptr(), sx.data_ptr(), 0, sp), "act_quant")
+        check(lib.fp8_act_quant(x.data_ptr(), fp8.BF16, Mt, Kh, qx.data_ptr(), sx.data_ptr(), 0, cur()), "act_quant")
         dw = torch.empty((Nf, Kh), dtype=torch.float32, device=dev)
         qbytes = lambda r, c: r * c * 3 + r * c // 128 * 4  # noqa: E731
         ops += [
             ("act_quant_dY", lambda: check(lib.fp8_act_quant(dy.data_ptr(), fp8.BF16, Mt, Nf, qd.data_ptr(),
-                                                             sd.data_ptr(), 0, sp), "act_quant"),
+                                                             sd.data_ptr(), 0, cur()), "act_quant"),
              "hbm", qbytes(Mt, Nf)),
             ("act_quant_T_dY", lambda: check(lib.fp8_act_quant(dy.data_ptr(), fp8.BF16, Mt, Nf, qdt.data_ptr(),
-                                                               sdt.data_ptr(), fp8.TRANSPOSE, sp), "act_quant_T"),
+                                                               sdt.data_ptr(), fp8.TRANSPOSE, cur()), "act_quant_T"),
              "hbm", qbytes(Mt, Nf)),
             ("requant_T_X_stored", lambda: check(lib.fp8_requant_transpose(
-                qx.data_ptr(), sx.data_ptr(), Mt, Kh, qxt.data_ptr(), sxt.data_ptr(), 0, sp), "requant_T"),
+                qx.data_ptr(), sx.data_ptr(), Mt, Kh, qxt.data_ptr(), sxt.data_ptr(), 0, cur()), "requant_T"),
              "hbm", Mt * Kh * 2 + Mt * (Kh // 128) * 4 + Kh * (Mt // 128) * 4),
             ("weight_quant_W_with_T", lambda: check(lib.fp8_weight_quant(
                 w.data_ptr(), fp8.BF16, Nf, Kh, qw.data_ptr(), sw.data_ptr(), qwt.data_ptr(), swt.data_ptr(),
-                0, sp), "weight_quant"),
+                0, cur()), "weight_quant"),
              "hbm", Nf * Kh * 4 + 2 * (Nf // 128) * (Kh // 128) * 4),
             ("gemm_dgrad", lambda: check(lib.fp8_blockscaled_gemm(
                 qd.data_ptr(), sd.data_ptr(), qwt.data_ptr(), swt.data_ptr(), dx.data_ptr(), fp8.BF16,
-                Mt, Kh, Nf, 0, sp), "dgrad"),
+                Mt, Kh, Nf, 0, cur()), "dgrad"),
              "tensor", 2 * Mt * Kh * Nf),
             ("gemm_wgrad", lambda: check(lib.fp8_blockscaled_gemm(
                 qdt.data_ptr(), sdt.data_ptr(), qxt.data_ptr(), sxt.data_ptr(), dw.data_ptr(), fp8.F32,
-                Nf, Kh, Mt, fp8.B_TILE1x128, sp), "wgrad"),
+                Nf, Kh, Mt, fp8.B_TILE1x128, cur()), "wgrad"),
              "tensor", 2 * Nf * Kh * Mt),
         ]
         desc = {"workload": "backward_ffn_dy4096x18432_x4096x7168_w18432x7168",
@@ -547,11 +576,11 @@ def run_workload(args, rank, world):
 
         def wq_up():
             check(lib.fp8_weight_quant(wu.data_ptr(), fp8.BF16, E * 2 * I, H, qu.data_ptr(), su.data_ptr(),
-                                       None, None, 0, sp), "weight_quant up")
+                                       None, None, 0, cur()), "weight_quant up")
 
         def wq_down():
             check(lib.fp8_weight_quant(wd.data_ptr(), fp8.BF16, E * H, I, qdn.data_ptr(), sdn.data_ptr(),
-                                       None, None, 0, sp), "weight_quant down")
+                                       None, None, 0, cur()), "weight_quant down")
 
         wq_up()
         wq_down()
@@ -559,7 +588,7 @@ def run_workload(args, rank, world):
         qh, sh = u8(T, I), f32(T, I // 128)
         up = torch.empty((T, 2 * I), dtype=torch.bfloat16, device=dev)
         down = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
-        check(lib.fp8_act_quant(tok.data_ptr(), fp8.BF16, case.T, H, qt.data_ptr(), st.data_ptr(), fp8.POW2, sp),
+        check(lib.fp8_act_quant(tok.data_ptr(), fp8.BF16, case.T, H, qt.data_ptr(), st.data_ptr(), fp8.POW2, cur()),
               "act_quant")
         # dispatch (row gather in expert order) is routing glue: done once, outside the timed step
         qa, sa = qt.index_select(0, idx).contiguous(), st.index_select(0, idx).contiguous()
@@ -567,15 +596,15 @@ def run_workload(args, rank, world):
         up_bytes = E * 2 * I * H + E * (2 * I // 128) * (H // 128) * 4 + T * H + T * H // 128 * 4
         ops += [
             ("act_quant_tokens_pow2", lambda: check(lib.fp8_act_quant(
-                tok.data_ptr(), fp8.BF16, case.T, H, qt.data_ptr(), st.data_ptr(), fp8.POW2, sp), "act_quant"),
+                tok.data_ptr(), fp8.BF16, case.T, H, qt.data_ptr(), st.data_ptr(), fp8.POW2, cur()), "act_quant"),
              "hbm", case.T * H * 3 + case.T * H // 128 * 4),
             ("grouped_up_swiglu", lambda: check(lib.fp8_grouped_gemm_swiglu_quant(
                 qa.data_ptr(), sa.data_ptr(), off.data_ptr(), E, T, qu.data_ptr(), su.data_ptr(), qh.data_ptr(),
-                sh.data_ptr(), 2 * I, H, fp8.POW2, sp), "grouped_up_swiglu"),
+                sh.data_ptr(), 2 * I, H, fp8.POW2, cur()), "grouped_up_swiglu"),
              "hbm", up_bytes + T * I + T * I // 128 * 4),
             ("grouped_down", lambda: check(lib.fp8_grouped_gemm(
                 qh.data_ptr(), sh.data_ptr(), off.data_ptr(), E, T, qdn.data_ptr(), sdn.data_ptr(), down.data_ptr(),
-                fp8.BF16, H, I, 0, sp), "grouped_down"),
+                fp8.BF16, H, I, 0, cur()), "grouped_down"),
              "hbm", E * H * I + E * (H // 128) * (I // 128) * 4 + T * I + T * I // 128 * 4 + T * H * 2),
         ]
         # the unfused producer of the down-projection input, timed apart for comparison
@@ -584,10 +613,10 @@ def run_workload(args, rank, world):
         compare_ops = [
             ("unfused_grouped_up_bf16", lambda: check(lib.fp8_grouped_gemm(
                 qa.data_ptr(), sa.data_ptr(), off.data_ptr(), E, T, qu.data_ptr(), su.data_ptr(), up.data_ptr(),
-                fp8.BF16, 2 * I, H, 0, sp), "grouped_up"),
+                fp8.BF16, 2 * I, H, 0, cur()), "grouped_up"),
              "hbm", up_bytes + T * 2 * I * 2),
             ("unfused_act_quant_h_pow2", lambda: check(lib.fp8_act_quant(
-                h_bf16.data_ptr(), fp8.BF16, T, I, qh2.data_ptr(), sh2.data_ptr(), fp8.POW2, sp), "act_quant"),
+                h_bf16.data_ptr(), fp8.BF16, T, I, qh2.data_ptr(), sh2.data_ptr(), fp8.POW2, cur()), "act_quant"),
              "hbm", T * I * 3 + T * I // 128 * 4),
             ("expert_weight_quant_up_all", wq_up, "hbm", E * 2 * I * H * 3 + E * (2 * I // 128) * (H // 128) * 4),
             ("expert_weight_quant_down_all", wq_down, "hbm", E * H * I * 3 + E * (H // 128) * (I // 128) * 4),
@@ -615,23 +644,23 @@ def run_workload(args, rank, world):
         x, w = case.x().to(dev), case.w().to(dev)
         qx, sx = u8(Mt, Kh), f32(Mt, Kh // 128)
         qw, sw = u8(Nf, Kh), f32(Nf // 128, Kh // 128)
-        check(lib.fp8_act_quant(x.data_ptr(), fp8.BF16, Mt, Kh, qx.data_ptr(), sx.data_ptr(), 0, sp), "act_quant")
+        check(lib.fp8_act_quant(x.data_ptr(), fp8.BF16, Mt, Kh, qx.data_ptr(), sx.data_ptr(), 0, cur()), "act_quant")
         check(lib.fp8_weight_quant(w.data_ptr(), fp8.BF16, Nf, Kh, qw.data_ptr(), sw.data_ptr(), None, None, 0,
-                                   sp), "weight_quant")
+                                   cur()), "weight_quant")
         yb = torch.empty((Mt, Nf), dtype=torch.bfloat16, device=dev)
         qy, sy = u8(Mt, Nf), f32(Mt, Nf // 128)
         qy2, sy2 = u8(Mt, Nf), f32(Mt, Nf // 128)
         ops += [
             ("gemm_bf16", lambda: check(lib.fp8_blockscaled_gemm(
                 qx.data_ptr(), sx.data_ptr(), qw.data_ptr(), sw.data_ptr(), yb.data_ptr(), fp8.BF16,
-                Mt, Nf, Kh, 0, sp), "gemm"),
+                Mt, Nf, Kh, 0, cur()), "gemm"),
              "tensor", 2 * Mt * Nf * Kh),
             ("act_quant_Y", lambda: check(lib.fp8_act_quant(
-                yb.data_ptr(), fp8.BF16, Mt, Nf, qy.data_ptr(), sy.data_ptr(), 0, sp), "act_quant"),
+                yb.data_ptr(), fp8.BF16, Mt, Nf, qy.data_ptr(), sy.data_ptr(), 0, cur()), "act_quant"),
              "hbm", Mt * Nf * 3 + Mt * Nf // 128 * 4),
             ("gemm_quant_fused", lambda: check(lib.fp8_blockscaled_gemm_quant(
                 qx.data_ptr(), sx.data_ptr(), qw.data_ptr(), sw.data_ptr(), qy2.data_ptr(), sy2.data_ptr(),
-                Mt, Nf, Kh, 0, sp), "gemm_quant"),
+                Mt, Nf, Kh, 0, cur()), "gemm_quant"),
              "tensor", 2 * Mt * Nf * Kh),
         ]
         desc = {"workload": "producer_fprop_x4096x7168_w18432x7168",
@@ -639,33 +668,35 @@ def run_workload(args, rank, world):
                         "E4M3 quantisation in its epilogue (both per step; value counts both GEMMs)",
                 "data": "synthetic (seeded N(0,1) X with 0.1% x100 outliers, N(0,0.02) W)"}
     else:  # ksweep
+        ncopy = 4      # rotating input copies: 4 x (16-64 MB) per K, above the 126 MB L2
         for Kk in (4096, 8192, 16384):
             cs = synth.dense_case(f"ksweep{Kk}")
-            xx, ww = cs.x().to(dev), cs.w().to(dev)
+            xx0, ww0 = cs.x().to(dev), cs.w().to(dev)
             Mm, Nn = cs.M, cs.N
-            qa_, sa_ = u8(Mm, Kk), f32(Mm, Kk // 128)
-            qb_, sb_ = u8(Nn, Kk), f32(Nn // 128, Kk // 128)
-            cc = torch.empty((Mm, Nn), dtype=torch.float32, device=dev)
-
-            def mk(xx=xx, ww=ww, qa_=qa_, sa_=sa_, qb_=qb_, sb_=sb_, cc=cc, Mm=Mm, Nn=Nn, Kk=Kk):
-                return [
-                    (f"act_quant_k{Kk}", lambda: check(lib.fp8_act_quant(
-                        xx.data_ptr(), fp8.BF16, Mm, Kk, qa_.data_ptr(), sa_.data_ptr(), 0, sp), "act_quant"),
-                     "hbm", Mm * Kk * 3 + Mm * Kk // 128 * 4),
-                    (f"weight_quant_k{Kk}", lambda: check(lib.fp8_weight_quant(
-                        ww.data_ptr(), fp8.BF16, Nn, Kk, qb_.data_ptr(), sb_.data_ptr(), None, None, 0, sp),
-                        "weight_quant"),
-                     "hbm", Nn * Kk * 3 + (Nn // 128) * (Kk // 128) * 4),
-                    (f"gemm_k{Kk}", lambda: check(lib.fp8_blockscaled_gemm(
-                        qa_.data_ptr(), sa_.data_ptr(), qb_.data_ptr(), sb_.data_ptr(), cc.data_ptr(), fp8.F32,
-                        Mm, Nn, Kk, 0, sp), "gemm"),
-                     "tensor", 2 * Mm * Nn * Kk),
-                ]
-            ops += mk()
+            fa, fw, fg = [], [], []
+            for _ in range(ncopy):
+                xx, ww = xx0.clone(), ww0.clone()
+                qa_, sa_ = u8(Mm, Kk), f32(Mm, Kk // 128)
+                qb_, sb_ = u8(Nn, Kk), f32(Nn // 128, Kk // 128)
+                cc = torch.empty((Mm, Nn), dtype=torch.float32, device=dev)
+                fa.append(lambda xx=xx, qa_=qa_, sa_=sa_, Mm=Mm, Kk=Kk: check(lib.fp8_act_quant(
+                    xx.data_ptr(), fp8.BF16, Mm, Kk, qa_.data_ptr(), sa_.data_ptr(), 0, cur()), "act_quant"))
+                fw.append(lambda ww=ww, qb_=qb_, sb_=sb_, Nn=Nn, Kk=Kk: check(lib.fp8_weight_quant(
+                    ww.data_ptr(), fp8.BF16, Nn, Kk, qb_.data_ptr(), sb_.data_ptr(), None, None, 0, cur()),
+                    "weight_quant"))
+                fg.append(lambda qa_=qa_, sa_=sa_, qb_=qb_, sb_=sb_, cc=cc, Mm=Mm, Nn=Nn, Kk=Kk: check(
+                    lib.fp8_blockscaled_gemm(qa_.data_ptr(), sa_.data_ptr(), qb_.data_ptr(), sb_.data_ptr(),
+                                             cc.data_ptr(), fp8.F32, Mm, Nn, Kk, 0, cur()), "gemm"))
+            ops += [
+                (f"act_quant_k{Kk}", fa, "hbm", Mm * Kk * 3 + Mm * Kk // 128 * 4),
+                (f"weight_quant_k{Kk}", fw, "hbm", Nn * Kk * 3 + (Nn // 128) * (Kk // 128) * 4),
+                (f"gemm_k{Kk}", fg, "tensor", 2 * Mm * Nn * Kk),
+            ]
         desc = {"workload": "ksweep_2048x2048_k4096_8192_16384",
                 "step": "per K: act_quant X + weight_quant W + gemm -> f32",
                 "data": "synthetic: X, W N(0,1) with 0.5% Student-t(2) replacements",
-                "l2": "working set 2-4x smaller than L2 for K <= 8192: these times include L2 hits"}
+                "l2": f"{ncopy} rotating copies of every input and output per K; step i uses copy i % {ncopy}, "
+                      "so consecutive steps touch 4x the per-K working set (64-256 MB, above the 126 MB L2)"}
 
     steps = args.steps
     total_ms, per, clocks = _timed_loop([(n, f) for n, f, _, _ in ops], steps, args.warmup, stream, dev,
@@ -715,6 +746,8 @@ def run_workload(args, rank, world):
                 "traffic": None, "algorithmic_bytes": damount}
     cfg = dict(desc)
     cfg["parallelism"] = f"{world} independent replica(s)"
+    cfg["timing"] = ("every op replayed from its own CUDA graph; the timed region is enqueued behind a "
+                     "GPU-side wait, so the host is ahead of the GPU and per-op times are kernel times")
     return {
         "metric": METRIC, "value": round(job_rate(world, steps * gemm_flops, total_ms) / 1e12, 3),
         "unit": "TFLOP/s", "n_gpus": world, "steps": steps, "warmup": max(args.warmup, 3),
