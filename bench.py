@@ -301,6 +301,23 @@ def run_ours(args, rank, world):
     t_wq = statistics.mean(e[1].elapsed_time(e[2]) for e in evs)
     t_mm = statistics.mean(e[2].elapsed_time(e[3]) for e in evs)
     clocks = clk.summary("start", "end")
+    # Ramp floor of act_quant at this size: torch's plain BF16 -> E4M3 cast of the
+    # same X moves the same bytes per element (2 read, 1 written) with no scaling.
+    # It is timed in the same place in the step (right after a GEMM); it is a
+    # reference for the quantiser only, not part of the path.
+    floor_out = torch.empty((M, K), dtype=torch.float8_e4m3fn, device=dev)
+    fl = []
+    for i in range(max(args.steps, 5) + 3):
+        mm()
+        f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        f0.record(stream)
+        floor_out.copy_(x)
+        f1.record(stream)
+        torch.cuda.synchronize()
+        if i >= 3:
+            fl.append(f0.elapsed_time(f1))
+    t_floor = statistics.mean(fl)
+    del floor_out
     # one second of the same step under the sampler: a clock record the GEMM
     # certainly covers, and the per-op times at the clock held under load
     window = None if args.no_clock_window else clock_window(
@@ -382,7 +399,12 @@ def run_ours(args, rank, world):
         "per_op": {
             "act_quant": {"ms": round(t_act, 5), "GB/s": round(aq_gbs, 1),
                           "frac_hbm": round(aq_gbs / hbm, 4), "frac_hbm_8tbs": round(aq_gbs / 8000.0, 4),
-                          "bytes": aq_bytes},
+                          "bytes": aq_bytes,
+                          "ramp_floor": {"what": "torch BF16->E4M3 cast of the same X (same bytes per "
+                                                 "element, no scaling), timed right after a GEMM",
+                                         "ms": round(t_floor, 5),
+                                         "GB/s": round(aq_bytes / (t_floor * 1e-3) / 1e9, 1),
+                                         "act_quant_frac_of_floor": round(t_floor / t_act, 4)}},
             "weight_quant": {"ms": round(t_wq, 5), "GB/s": round(wq_gbs, 1),
                              "frac_hbm": round(wq_gbs / hbm, 4),
                              "frac_hbm_8tbs": round(wq_gbs / 8000.0, 4), "bytes": wq_bytes},

@@ -319,12 +319,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             if constexpr (EPI == EPI_SWIGLU) {
               // B rows of the stage: gate j0..j0+63, up j0.., gate j0+64.., up j0+64..
               // (j0 = n0/2), so each TMEM column half holds g and u of the same
-              // 64 outputs
-              const int j0 = tl.n0 / 2;
-#pragma unroll
-              for (int i = 0; i < 4; ++i)
-                tma_load_3d(smem_u32(sm.b[stage]) + i * (B_BYTES / 4), &tmB, fb, kb * BK,
-                            (i & 1) * (p.N / 2) + j0 + (i >> 1) * 64, tl.e);
+              // 64 outputs.  One request over the 5-D view {K, 64 rows, gate/up,
+              // 64-row block, expert} of B lands them in that order (four
+              // 64-row requests measured 5 % slower for the kernel).
+              tma_load_5d(smem_u32(sm.b[stage]), &tmB, fb, kb * BK, 0, 0, tl.n0 / 128, tl.e);
             } else if constexpr (GROUPED)
               tma_load_3d(smem_u32(sm.b[stage]), &tmB, fb, kb * BK, tl.n0, tl.e);
             else
@@ -1022,9 +1020,17 @@ fp8fg_status launch_grouped_swiglu_quant(const uint8_t* a, const float* sa,
                                          const uint8_t* b, const float* sb, uint8_t* q, float* s,
                                          int64_t N, int64_t K, bool pow2, cudaStream_t st) {
   CUtensorMap mA, mB;
-  // B is read as four 64-row boxes per stage (gate, up, gate, up)
-  if (!make_maps(&mA, &mB, a, total_rows > 0 ? total_rows : 1, b, E, N, K, BN / 4))
-    return FP8FG_ERR_CUDA;
+  if (!make_maps(&mA, &mB, a, total_rows > 0 ? total_rows : 1, b, E, N, K)) return FP8FG_ERR_CUDA;
+  // B as a 5-D view of [E, N = 2I, K]: {K, 64 rows, gate/up (stride I rows),
+  // 64-row block (stride 64 rows), expert}; a box of {128, 64, 2, 2, 1} is one
+  // pipeline stage: gate and up rows of 128 outputs, 64 at a time
+  {
+    const uint64_t I = static_cast<uint64_t>(N / 2), Ku = static_cast<uint64_t>(K);
+    const uint64_t dB[5] = {Ku, 64, 2, I / 64, static_cast<uint64_t>(E)};
+    const uint64_t sB[4] = {Ku, I * Ku, 64 * Ku, 2 * I * Ku};
+    const uint32_t boxB[5] = {BK, 64, 2, 2, 1};
+    if (!encode_tensor_map_u8(&mB, b, 5, dB, sB, boxB)) return FP8FG_ERR_CUDA;
+  }
   if (set_smem_attr<true, false, EPI_SWIGLU>() != cudaSuccess) return FP8FG_ERR_CUDA;
   GemmParams p{};
   p.sa = sa;
