@@ -633,6 +633,12 @@ def run_workload(args, rank, world):
         h_bf16 = synth.swiglu_like_bf16((T, I), case.seed).to(dev)
         qh2, sh2 = u8(T, I), f32(T, I // 128)
         compare_ops = [
+            # the fused kernel again, so that both producers are timed in one loop
+            # under the same clock (the step loop runs at a different power level)
+            ("fused_up_swiglu_same_loop", lambda: check(lib.fp8_grouped_gemm_swiglu_quant(
+                qa.data_ptr(), sa.data_ptr(), off.data_ptr(), E, T, qu.data_ptr(), su.data_ptr(), qh.data_ptr(),
+                sh.data_ptr(), 2 * I, H, fp8.POW2, cur()), "grouped_up_swiglu"),
+             "hbm", up_bytes + T * I + T * I // 128 * 4),
             ("unfused_grouped_up_bf16", lambda: check(lib.fp8_grouped_gemm(
                 qa.data_ptr(), sa.data_ptr(), off.data_ptr(), E, T, qu.data_ptr(), su.data_ptr(), up.data_ptr(),
                 fp8.BF16, 2 * I, H, 0, cur()), "grouped_up"),
@@ -651,13 +657,14 @@ def run_workload(args, rank, world):
                            f"{int(r['counts'].max())}; row gather done once outside the timed step",
                 "data": "synthetic: tokens N(0,1), router N(0,0.02^2), bias U(-0.1,0.1), experts N(0,0.02^2); "
                         "the down-projection input is the fused up-projection's h",
-                "compare": "unfused producer (grouped up -> bf16, then act_quant of an h-shaped bf16 tensor) "
-                           "timed in a separate loop: per_op unfused_*",
+                "compare": "fused producer and unfused producer (grouped up -> bf16, then act_quant of an "
+                           "h-shaped bf16 tensor) timed together in a separate loop: per_op "
+                           "fused_up_swiglu_same_loop and unfused_*",
                 "weights": "expert weights quantised once before the timed step, not per step; re-quantising "
                            "all 256 experts' BF16 weights (22.5 GB read, 11.3 GB written) is timed in the "
                            "separate loop: per_op expert_weight_quant_up_all / _down_all"}
         flops = {"grouped_up_swiglu": 2 * T * 2 * I * H, "grouped_down": 2 * T * H * I,
-                 "unfused_grouped_up_bf16": 2 * T * 2 * I * H}
+                 "fused_up_swiglu_same_loop": 2 * T * 2 * I * H, "unfused_grouped_up_bf16": 2 * T * 2 * I * H}
     elif args.workload == "producer":
         # the Fprop GEMM as the producer of the next FP8 GEMM's input: BF16 out
         # then act_quant of it, against the fused E4M3 epilogue
