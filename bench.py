@@ -549,6 +549,9 @@ def run_workload(args, rank, world):
         qx, sx = u8(Mt, Kh), f32(Mt, Kh // 128)
         check(lib.fp8_act_quant(x.data_ptr(), fp8.BF16, Mt, Kh, qx.data_ptr(), sx.data_ptr(), 0, cur()), "act_quant")
         dw = torch.empty((Nf, Kh), dtype=torch.float32, device=dev)
+        # stream-K workspace for Dgrad (896 output tiles leave most SMs idle in the last wave)
+        ws_bytes = lib.fp8_blockscaled_gemm_workspace_bytes(Mt, Kh, Nf, 0)
+        ws_dgrad = torch.empty(ws_bytes, dtype=torch.uint8, device=dev) if ws_bytes else None
         qbytes = lambda r, c: r * c * 3 + r * c // 128 * 4  # noqa: E731
         ops += [
             ("act_quant_dY", lambda: check(lib.fp8_act_quant(dy.data_ptr(), fp8.BF16, Mt, Nf, qd.data_ptr(),
@@ -564,9 +567,10 @@ def run_workload(args, rank, world):
                 w.data_ptr(), fp8.BF16, Nf, Kh, qw.data_ptr(), sw.data_ptr(), qwt.data_ptr(), swt.data_ptr(),
                 0, cur()), "weight_quant"),
              "hbm", Nf * Kh * 4 + 2 * (Nf // 128) * (Kh // 128) * 4),
-            ("gemm_dgrad", lambda: check(lib.fp8_blockscaled_gemm(
+            ("gemm_dgrad", lambda: check(lib.fp8_blockscaled_gemm_ws(
                 qd.data_ptr(), sd.data_ptr(), qwt.data_ptr(), swt.data_ptr(), dx.data_ptr(), fp8.BF16,
-                Mt, Kh, Nf, 0, cur()), "dgrad"),
+                Mt, Kh, Nf, 0, ws_dgrad.data_ptr() if ws_dgrad is not None else None,
+                0 if ws_dgrad is None else ws_dgrad.numel(), cur()), "dgrad"),
              "tensor", 2 * Mt * Kh * Nf),
             ("gemm_wgrad", lambda: check(lib.fp8_blockscaled_gemm(
                 qdt.data_ptr(), sdt.data_ptr(), qxt.data_ptr(), sxt.data_ptr(), dw.data_ptr(), fp8.F32,
@@ -575,8 +579,8 @@ def run_workload(args, rank, world):
         ]
         desc = {"workload": "backward_ffn_dy4096x18432_x4096x7168_w18432x7168",
                 "step": "act_quant dY (1x128) + 128x1 quant of dY + 128x1 re-quantisation of the stored "
-                        "FP8 X + weight_quant W with W^T + Dgrad dY.W -> bf16 [4096,7168] "
-                        "+ Wgrad dY^T.X -> f32 [18432,7168]",
+                        "FP8 X + weight_quant W with W^T + Dgrad dY.W -> bf16 [4096,7168] (stream-K split "
+                        "of the leftover tiles, fix-up kernel included) + Wgrad dY^T.X -> f32 [18432,7168]",
                 "data": "synthetic: dY N(0,1e-3^2), X N(0,1) 0.1% x100, W N(0,0.02^2)"}
     elif args.workload == "moe":
         case = synth.MOE_FULL

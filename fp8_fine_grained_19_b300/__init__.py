@@ -20,13 +20,14 @@ __all__ = [
     "gemm_quant", "grouped_gemm", "grouped_swiglu_quant",
     "device_status", "set_wait_limit", "selftest_wait_timeout", "status_string",
     "OK", "ERR_INVALID_ARG", "ERR_UNSUPPORTED_SHAPE", "ERR_MISALIGNED", "ERR_CUDA",
-    "ERR_TIMEOUT", "ERR_BAD_OFFSETS", "POW2", "TRANSPOSE", "B_TILE1x128", "WHOLE_K", "BF16", "F32",
+    "ERR_TIMEOUT", "ERR_BAD_OFFSETS", "POW2", "TRANSPOSE", "B_TILE1x128", "WHOLE_K", "STREAM_K",
+    "BF16", "F32", "gemm_workspace_bytes",
 ]
 
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED_SHAPE, ERR_MISALIGNED, ERR_CUDA, ERR_TIMEOUT, \
     ERR_BAD_OFFSETS = range(7)
 BF16, F32 = 0, 1
-POW2, TRANSPOSE, B_TILE1x128, WHOLE_K = 1, 2, 4, 8
+POW2, TRANSPOSE, B_TILE1x128, WHOLE_K, STREAM_K = 1, 2, 4, 8, 16
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _LIB: ctypes.CDLL | None = None
@@ -37,6 +38,9 @@ _SIGS = {
     "fp8_weight_quant": [_vp, ctypes.c_int, _i64, _i64, _vp, _vp, _vp, _vp, _u32, _vp],
     "fp8_requant_transpose": [_vp, _vp, _i64, _i64, _vp, _vp, _u32, _vp],
     "fp8_blockscaled_gemm": [_vp, _vp, _vp, _vp, _vp, ctypes.c_int, _i64, _i64, _i64, _u32, _vp],
+    "fp8_blockscaled_gemm_ws": [_vp, _vp, _vp, _vp, _vp, ctypes.c_int, _i64, _i64, _i64, _u32, _vp,
+                                ctypes.c_size_t, _vp],
+    "fp8_blockscaled_gemm_workspace_bytes": [_i64, _i64, _i64, _u32],
     "fp8_blockscaled_gemm_quant": [_vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _u32, _vp],
     "fp8_grouped_gemm": [_vp, _vp, _vp, _i32, _i64, _vp, _vp, _vp, ctypes.c_int, _i64, _i64,
                          _u32, _vp],
@@ -74,7 +78,8 @@ def load() -> ctypes.CDLL:
         f = getattr(lib, name)
         f.argtypes = args
         f.restype = ctypes.c_char_p if name == "fp8fg_status_string" else (
-            None if name == "fp8fg_set_wait_limit" else ctypes.c_int)
+            None if name == "fp8fg_set_wait_limit" else (
+                ctypes.c_size_t if name == "fp8_blockscaled_gemm_workspace_bytes" else ctypes.c_int))
     _LIB = lib
     return lib
 
@@ -191,12 +196,24 @@ def _out_code(dtype) -> int:
     raise ValueError(f"unsupported output dtype {dtype}")
 
 
+def gemm_workspace_bytes(M: int, N: int, K: int, b_tile: bool = False, stream_k: bool = False,
+                         device=None) -> int:
+    """Workspace bytes the stream-K split of this GEMM uses on `device` (0: no split)."""
+    flags = (B_TILE1x128 if b_tile else 0) | (STREAM_K if stream_k else 0)
+    dev = _device_arg(device)
+    with torch.cuda.device(dev):
+        return int(load().fp8_blockscaled_gemm_workspace_bytes(M, N, K, flags))
+
+
 def gemm(a, sa, b, sb, out_dtype=torch.bfloat16, b_tile: bool = False, out=None, stream=None,
-         whole_k: bool = False):
+         whole_k: bool = False, stream_k="auto", workspace=None):
     """C[M, N] = sum_kb (A_kb . B_kb^T) * sa[:, kb] * sb(., kb), promoted to FP32 per 128 K.
 
     whole_k: study mode without promotion (all of K in the tensor core, scaled by
-    sa[0, 0] * sb[0, 0])."""
+    sa[0, 0] * sb[0, 0]).
+    stream_k: "auto" splits the K slices of the last tiles among all SMs when the
+    tiles would leave most SMs idle (a workspace is then taken from torch, or
+    `workspace` is used); True forces the split; False never splits."""
     for t, n in ((a, "a"), (b, "b")):
         _need(t, (torch.uint8,), n)
     for t, n in ((sa, "sa"), (sb, "sb")):
@@ -210,9 +227,24 @@ def gemm(a, sa, b, sb, out_dtype=torch.bfloat16, b_tile: bool = False, out=None,
         out = torch.empty((M, N), dtype=out_dtype, device=dev)
     _need(out, (torch.bfloat16, torch.float32), "out")
     flags = (B_TILE1x128 if b_tile else 0) | (WHOLE_K if whole_k else 0)
-    _check(_run("fp8_blockscaled_gemm", dev, _ptr(a), _ptr(sa), _ptr(b), _ptr(sb), _ptr(out),
-                _out_code(out.dtype), M, N, K, flags, _stream(stream, dev)),
-           "fp8_blockscaled_gemm")
+    if whole_k or stream_k is False:
+        _check(_run("fp8_blockscaled_gemm", dev, _ptr(a), _ptr(sa), _ptr(b), _ptr(sb), _ptr(out),
+                    _out_code(out.dtype), M, N, K, flags, _stream(stream, dev)),
+               "fp8_blockscaled_gemm")
+        return out
+    if stream_k is True:
+        flags |= STREAM_K
+    need = gemm_workspace_bytes(M, N, K, b_tile, stream_k is True, dev) if M > 0 else 0
+    if need and workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+    if workspace is not None:
+        _need(workspace, (torch.uint8,), "workspace")
+        if workspace.device != dev:
+            raise ValueError("workspace must be on the device of the operands")
+    _check(_run("fp8_blockscaled_gemm_ws", dev, _ptr(a), _ptr(sa), _ptr(b), _ptr(sb), _ptr(out),
+                _out_code(out.dtype), M, N, K, flags, _ptr(workspace) if need else None,
+                workspace.numel() if (need and workspace is not None) else 0, _stream(stream, dev)),
+           "fp8_blockscaled_gemm_ws")
     return out
 
 

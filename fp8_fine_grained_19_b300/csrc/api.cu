@@ -132,7 +132,7 @@ bool have_device() { return device_sm_count() > 0; }
 
 extern "C" {
 
-int fp8fg_abi_version(void) { return 5; }
+int fp8fg_abi_version(void) { return 6; }
 
 const char* fp8fg_status_string(fp8fg_status status) {
   switch (status) {
@@ -197,13 +197,16 @@ fp8fg_status fp8_weight_quant(const void* w, fp8fg_dtype w_dtype, int64_t N, int
                                        (flags & FP8FG_POW2) != 0, as_stream(stream)));
 }
 
-fp8fg_status fp8_blockscaled_gemm(const uint8_t* a, const float* sa, const uint8_t* b,
-                                  const float* sb, void* c, fp8fg_dtype c_dtype, int64_t M,
-                                  int64_t N, int64_t K, unsigned flags, void* stream) {
-  if (!valid_dtype(c_dtype) || (flags & ~(FP8FG_B_TILE1x128 | FP8FG_WHOLE_K)) != 0 || M < 0 ||
-      N < 0 || K < 0)
+namespace {
+
+// Host checks shared by the dense GEMM entry points (no CUDA call).
+fp8fg_status check_gemm_args(const uint8_t* a, const float* sa, const uint8_t* b, const float* sb,
+                             void* c, fp8fg_dtype c_dtype, int64_t M, int64_t N, int64_t K,
+                             unsigned flags, unsigned allowed) {
+  if (!valid_dtype(c_dtype) || (flags & ~allowed) != 0 || M < 0 || N < 0 || K < 0)
     return FP8FG_ERR_INVALID_ARG;
   if ((flags & FP8FG_B_TILE1x128) && (flags & FP8FG_WHOLE_K)) return FP8FG_ERR_INVALID_ARG;
+  if ((flags & FP8FG_STREAM_K) && (flags & FP8FG_WHOLE_K)) return FP8FG_ERR_INVALID_ARG;
   if (b == nullptr || sb == nullptr || (M > 0 && (a == nullptr || sa == nullptr || c == nullptr)))
     return FP8FG_ERR_INVALID_ARG;
   const bool b_tile = (flags & FP8FG_B_TILE1x128) != 0;
@@ -213,10 +216,45 @@ fp8fg_status fp8_blockscaled_gemm(const uint8_t* a, const float* sa, const uint8
   if (((M + 127) / 128) * ((N + 255) / 256) > kMaxDim) return FP8FG_ERR_UNSUPPORTED_SHAPE;
   if (!aligned16(a) || !aligned16(sa) || !aligned16(b) || !aligned16(sb) || !aligned16(c))
     return FP8FG_ERR_MISALIGNED;
+  return FP8FG_OK;
+}
+
+}  // namespace
+
+fp8fg_status fp8_blockscaled_gemm(const uint8_t* a, const float* sa, const uint8_t* b,
+                                  const float* sb, void* c, fp8fg_dtype c_dtype, int64_t M,
+                                  int64_t N, int64_t K, unsigned flags, void* stream) {
+  const fp8fg_status chk = check_gemm_args(a, sa, b, sb, c, c_dtype, M, N, K, flags,
+                                           FP8FG_B_TILE1x128 | FP8FG_WHOLE_K);
+  if (chk != FP8FG_OK) return chk;
   if (M == 0) return FP8FG_OK;
   if (!have_device()) return FP8FG_ERR_CUDA;
-  return launch_gemm(a, sa, b, sb, c, c_dtype, M, N, K, b_tile, (flags & FP8FG_WHOLE_K) != 0,
-                     as_stream(stream));
+  return launch_gemm(a, sa, b, sb, c, c_dtype, M, N, K, (flags & FP8FG_B_TILE1x128) != 0,
+                     (flags & FP8FG_WHOLE_K) != 0, nullptr, 0, false, as_stream(stream));
+}
+
+size_t fp8_blockscaled_gemm_workspace_bytes(int64_t M, int64_t N, int64_t K, unsigned flags) {
+  if (M <= 0 || N <= 0 || K < 128 || K % 128 != 0 || (flags & FP8FG_WHOLE_K) || !have_device())
+    return 0;
+  return gemm_workspace_bytes(M, N, K, false, (flags & FP8FG_STREAM_K) != 0);
+}
+
+fp8fg_status fp8_blockscaled_gemm_ws(const uint8_t* a, const float* sa, const uint8_t* b,
+                                     const float* sb, void* c, fp8fg_dtype c_dtype, int64_t M,
+                                     int64_t N, int64_t K, unsigned flags, void* workspace,
+                                     size_t workspace_bytes, void* stream) {
+  const fp8fg_status chk = check_gemm_args(a, sa, b, sb, c, c_dtype, M, N, K, flags,
+                                           FP8FG_B_TILE1x128 | FP8FG_STREAM_K);
+  if (chk != FP8FG_OK) return chk;
+  if (!aligned16(workspace)) return FP8FG_ERR_MISALIGNED;
+  if ((flags & FP8FG_STREAM_K) && workspace == nullptr) return FP8FG_ERR_INVALID_ARG;
+  if (M == 0) return FP8FG_OK;
+  if (!have_device()) return FP8FG_ERR_CUDA;
+  const bool force = (flags & FP8FG_STREAM_K) != 0;
+  if (workspace != nullptr && workspace_bytes < gemm_workspace_bytes(M, N, K, false, force))
+    return FP8FG_ERR_INVALID_ARG;
+  return launch_gemm(a, sa, b, sb, c, c_dtype, M, N, K, (flags & FP8FG_B_TILE1x128) != 0, false,
+                     workspace, workspace_bytes, force, as_stream(stream));
 }
 
 fp8fg_status fp8_blockscaled_gemm_quant(const uint8_t* a, const float* sa, const uint8_t* b,

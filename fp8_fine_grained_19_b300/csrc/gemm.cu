@@ -121,6 +121,62 @@ struct GemmParams {
   int pow2_out;           // quantised output: power-of-2 scales
   long long wait_limit;
   int* status;            // library status word
+  // Work split (see WorkList): tiles [0, dp_tiles) are whole tiles taken
+  // round-robin; the 128-K slices of the tiles after them (sk_iters slices in
+  // all) are divided evenly among the CTAs (stream-K).  A tile whose slices
+  // fall to more than one CTA leaves FP32 partial sums in the workspace ws
+  // ([grid][2][BM][BN]); the fix-up kernel adds them up.
+  int dp_tiles = INT32_MAX;
+  long long sk_iters = 0;
+  int sk_grid = 0;        // grid size of the stream-K launch (the fix-up recomputes the split)
+};
+
+// One unit of a CTA's work: slices [kb0, kb1) of tile t.  slot -1: the whole
+// tile (its result goes to C); 0 or 1: a part of a tile split between CTAs,
+// whose partial sum goes to the CTA's workspace slot (0: the first unit of
+// its stream-K range, 1: the last).
+struct Work {
+  int t, kb0, kb1, slot;
+};
+
+// The sequence of units of this CTA, the same for every warp role.  Only the
+// dense kernels that store C (SK) split slices; the others take whole tiles
+// round-robin.  Slice positions are 32-bit (the host splits only when the
+// stream-K slices number fewer than 2^31).
+template <bool SK>
+struct WorkList {
+  int next_dp, x, lo, hi;
+  __device__ __forceinline__ void init(const GemmParams& p) {
+    next_dp = blockIdx.x;
+    if constexpr (SK) {
+      lo = static_cast<int>(p.sk_iters * blockIdx.x / gridDim.x);
+      hi = static_cast<int>(p.sk_iters * (blockIdx.x + 1) / gridDim.x);
+    } else {
+      lo = hi = 0;
+    }
+    x = lo;
+  }
+  __device__ __forceinline__ bool next(const GemmParams& p, int num_tiles, Work& w) {
+    if (next_dp < min(p.dp_tiles, num_tiles)) {
+      w = {next_dp, 0, p.nkb, -1};
+      next_dp += gridDim.x;
+      return true;
+    }
+    if constexpr (!SK) {
+      return false;
+    } else {
+      if (x >= hi) return false;
+      const int j = x / p.nkb;
+      const int kb0 = x - j * p.nkb;
+      const int kb1 = hi - x < p.nkb - kb0 ? kb0 + (hi - x) : p.nkb;
+      w.t = p.dp_tiles + j;
+      w.kb0 = kb0;
+      w.kb1 = kb1;
+      w.slot = (kb0 == 0 && kb1 == p.nkb) ? -1 : (x == lo ? 0 : 1);
+      x += kb1 - kb0;
+      return true;
+    }
+  }
 };
 
 // Shared memory of one CTA.  The expert tables exist only in the grouped
@@ -173,21 +229,29 @@ struct Tile {
   int e;        // expert (0 when dense)
 };
 
+// Tile t of a dense launch: groups of group_m M-tiles, all N-tiles of a group
+// before the next group, M fastest inside a group.
+__host__ __device__ __forceinline__ Tile dense_tile(int t, const GemmParams& p) {
+  Tile r;
+  const int group = p.group_m * p.n_tiles;
+  const int g = t / group;
+  const int first = g * p.group_m;
+  const int gm = min(p.group_m, p.m_tiles - first);
+  const int local = t - g * group;
+  const int mb = first + local % gm;
+  const int nb = local / gm;
+  r.m0 = mb * BM;
+  r.row_end = p.M;
+  r.n0 = nb * BN;
+  r.e = 0;
+  return r;
+}
+
 template <bool GROUPED, class S>
 __device__ __forceinline__ Tile tile_of(int t, const GemmParams& p, const S& sm) {
   Tile r;
   if constexpr (!GROUPED) {
-    const int group = p.group_m * p.n_tiles;
-    const int g = t / group;
-    const int first = g * p.group_m;
-    const int gm = min(p.group_m, p.m_tiles - first);
-    const int local = t - g * group;
-    const int mb = first + local % gm;
-    const int nb = local / gm;
-    r.m0 = mb * BM;
-    r.row_end = p.M;
-    r.n0 = nb * BN;
-    r.e = 0;
+    r = dense_tile(t, p);
   } else {
     // largest e with cum[e] <= t (experts with no tiles have cum[e] == cum[e+1])
     int lo = 0, hi = p.E - 1;
@@ -213,10 +277,12 @@ template <bool GROUPED, bool BTILE, int EPI>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     blockscaled_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                             const __grid_constant__ CUtensorMap tmB,
-                            const __grid_constant__ CUtensorMap tmC, const GemmParams p) {
+                            const __grid_constant__ CUtensorMap tmC,
+                            const __grid_constant__ CUtensorMap tmW, const GemmParams p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   // 1024-byte alignment of the operand stages (required by the 128B swizzle)
   using Smem = SmemT<GROUPED, BTILE>;
+  constexpr bool SKOK = !GROUPED && EPI == EPI_STORE;   // may split slices (stream-K)
   Smem& sm = *reinterpret_cast<Smem*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
 
@@ -247,6 +313,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
     tma_prefetch_desc(&tmC);
+    if (p.sk_iters > 0) tma_prefetch_desc(&tmW);
   }
   if constexpr (GROUPED) {
     // Copy and check the offsets, then prefix the per-expert tile counts with
@@ -307,9 +374,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         int stage = 0;
         uint32_t phase = 0;
         uint32_t issued = 0, issued_parity = 0;   // per-stage bits
-        for (int t = blockIdx.x; t < num_tiles && !*abort_flag; t += gridDim.x) {
-          const Tile tl = tile_of<GROUPED>(t, p, sm);
-          for (int kb = 0; kb < nkb; ++kb) {
+        WorkList<SKOK> wl;
+        wl.init(p);
+        Work wk;
+        while (!*abort_flag && wl.next(p, num_tiles, wk)) {
+          const Tile tl = tile_of<GROUPED>(wk.t, p, sm);
+          for (int kb = wk.kb0; kb < wk.kb1; ++kb) {
             if (!mbar_wait(smem_u32(&sm.empty_bar[stage]), phase ^ 1, p.wait_limit, abort_flag,
                            p.status))
               break;
@@ -348,8 +418,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       uint32_t it = 0;                              // slice counter (TMEM buffers)
       uint32_t tcount = 0;                          // tile counter (study mode buffers)
       bool ok = true;
-      for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x, ++tcount) {
-        for (int kb = 0; kb < nkb; ++kb, ++it) {
+      WorkList<SKOK> wl;
+      wl.init(p);
+      Work wk;
+      while (ok && wl.next(p, num_tiles, wk)) {
+        for (int kb = wk.kb0; kb < wk.kb1; ++kb, ++it) {
           const uint32_t ix = EPI == EPI_WHOLEK ? tcount : it;
           const uint32_t buf = ix & 1, bpar = (ix >> 1) & 1;
           int got = 0;
@@ -376,6 +449,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           if (EPI != EPI_WHOLEK || kb == nkb - 1) mma_commit_elect(smem_u32(&sm.tfull_bar[buf]));
           if (++stage == STAGES) { stage = 0; phase ^= 1; }
         }
+        ++tcount;
       }
       // all issued MMAs must finish before TMEM is released
       mma_commit_elect(smem_u32(&sm.drain_bar));
@@ -391,9 +465,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       // pairs.  Columns past N read the last column's scales (never stored).
       uint32_t grp = 0;
       bool live = true;
-      for (int t = blockIdx.x; t < num_tiles && live; t += gridDim.x) {
-        const Tile tl = tile_of<GROUPED>(t, p, sm);
-        for (int kb0 = 0; kb0 < nkb; kb0 += SB, ++grp) {
+      WorkList<SKOK> wl;
+      wl.init(p);
+      Work wk;
+      while (live && wl.next(p, num_tiles, wk)) {
+        const Tile tl = tile_of<GROUPED>(wk.t, p, sm);
+        for (int kb0 = wk.kb0; kb0 < wk.kb1; kb0 += SB, ++grp) {
           const uint32_t slot = grp % SB_SLOTS;
           if (!mbar_wait(smem_u32(&sm.sempty_bar[slot]), ((grp / SB_SLOTS) & 1) ^ 1, p.wait_limit,
                          abort_flag, p.status)) {
@@ -406,7 +483,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             const float* col = p.sb + static_cast<int64_t>(min(tl.n0 + c, p.N - 1)) * nkb;
 #pragma unroll
             for (int q = 0; q < SB; ++q)
-              sm.sring[slot][q][c] = kb0 + q < nkb ? __ldg(col + kb0 + q) : 0.0f;
+              sm.sring[slot][q][c] = kb0 + q < wk.kb1 ? __ldg(col + kb0 + q) : 0.0f;
           }
           __syncwarp();
           if (lane == 0) mbar_arrive(smem_u32(&sm.sfull_bar[slot]));
@@ -425,8 +502,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     uint32_t sgrp = 0;                              // tile mode: scale-ring group counter
     bool staged = false;                            // a store of this warp may still read cst
     bool ok = true;
-    for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
-      const Tile tl = tile_of<GROUPED>(t, p, sm);
+    WorkList<SKOK> wl;
+    wl.init(p);
+    Work wk;
+    while (ok && wl.next(p, num_tiles, wk)) {
+      const Tile tl = tile_of<GROUPED>(wk.t, p, sm);
       const int row = tl.m0 + quad * 32 + lane;
       const bool row_ok = row < tl.row_end;
       const int col_h = tl.n0 + half * 128;         // first column of this half
@@ -449,16 +529,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         // slices of this tile's 256 columns; a warp waits for a slot before
         // its first slice and frees it after its last, so no barrier joins
         // the promotion warps.
-        float sa_next = __ldg(sa_row);
-        for (int kb = 0; kb < nkb; ++kb, ++it) {
+        float sa_next = __ldg(sa_row + wk.kb0);
+        for (int kb = wk.kb0; kb < wk.kb1; ++kb, ++it) {
           const uint32_t slot = sgrp % SB_SLOTS;
-          if (kb % SB == 0 && !mbar_wait(smem_u32(&sm.sfull_bar[slot]), (sgrp / SB_SLOTS) & 1,
-                                         p.wait_limit, abort_flag, p.status)) {
+          const int g = kb - wk.kb0;                  // slice within the unit (ring groups start at kb0)
+          if (g % SB == 0 && !mbar_wait(smem_u32(&sm.sfull_bar[slot]), (sgrp / SB_SLOTS) & 1,
+                                        p.wait_limit, abort_flag, p.status)) {
             ok = false;
             break;
           }
           const float sa_cur = sa_next;
-          if (kb + 1 < nkb) sa_next = __ldg(sa_row + kb + 1);
+          if (kb + 1 < wk.kb1) sa_next = __ldg(sa_row + kb + 1);
           const uint32_t buf = it & 1, bpar = (it >> 1) & 1;
           if (!mbar_wait(smem_u32(&sm.tfull_bar[buf]), bpar, p.wait_limit, abort_flag, p.status)) {
             ok = false;
@@ -467,7 +548,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           tc_fence_after();
           const uint32_t taddr = lane_taddr + buf * BN;
           const uint64_t sa2 = pack2(__float_as_uint(sa_cur), __float_as_uint(sa_cur));
-          const uint32_t sbv = smem_u32(&sm.sring[slot][kb % SB][half * 128]);
+          const uint32_t sbv = smem_u32(&sm.sring[slot][g % SB][half * 128]);
 #pragma unroll
           for (int c = 0; c < 4; ++c) {
             // the coefficients sa * sb[col] of this chunk are formed while its
@@ -489,7 +570,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(smem_u32(&sm.tempty_bar[buf]));
-          if (kb % SB == SB - 1 || kb == nkb - 1) {
+          if (g % SB == SB - 1 || kb == wk.kb1 - 1) {
             // this warp's reads of the slot are complete (their values were used above)
             if (lane == 0) mbar_arrive(smem_u32(&sm.sempty_bar[slot]));
             ++sgrp;
@@ -523,12 +604,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         // SwiGLU: columns 64..127 of the half are up rows, whose block scale
         // lies I/128 blocks after the gate block
         const float* sbu_ptr = sb_ptr + (EPI == EPI_SWIGLU ? (p.N / 256) * nkb : 0);
-        float sa_next = __ldg(sa_row);
-        float sb_next = __ldg(sb_ptr);
-        float sbu_next = EPI == EPI_SWIGLU ? __ldg(sbu_ptr) : 0.0f;
-        for (int kb = 0; kb < nkb; ++kb, ++it) {
+        float sa_next = __ldg(sa_row + wk.kb0);
+        float sb_next = __ldg(sb_ptr + wk.kb0);
+        float sbu_next = EPI == EPI_SWIGLU ? __ldg(sbu_ptr + wk.kb0) : 0.0f;
+        for (int kb = wk.kb0; kb < wk.kb1; ++kb, ++it) {
           const float sa_cur = sa_next, sb_cur = sb_next, sbu_cur = sbu_next;
-          if (kb + 1 < nkb) {
+          if (kb + 1 < wk.kb1) {
             sa_next = __ldg(sa_row + kb + 1);
             sb_next = __ldg(sb_ptr + kb + 1);
             if constexpr (EPI == EPI_SWIGLU) sbu_next = __ldg(sbu_ptr + kb + 1);
@@ -775,20 +856,26 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         // chunks of 64 bytes per row.  Chunk q of row `lane` goes to staging
         // row `lane`, its 16-byte unit u at unit u ^ ((lane/2) % 4) (the 64-byte
         // swizzle), so a warp's st.shared.v4 hits every bank once per 8 lanes;
-        // one TMA store writes the chunk and clips rows at or past M.
-        const int wrow0 = tl.m0 + quad * 32;
-        if (half_ok && wrow0 < p.M) {
+        // one TMA store writes the chunk and clips rows at or past M.  A part
+        // of a tile split between CTAs (stream-K) goes whole, in FP32, to this
+        // CTA's workspace slot instead, for the fix-up kernel to add up.
+        const bool partial = wk.slot >= 0;
+        const bool f32 = partial || p.c_f32;
+        const int wrow0 = partial ? (static_cast<int>(blockIdx.x) * 2 + wk.slot) * BM + quad * 32
+                                  : tl.m0 + quad * 32;
+        const int wcol0 = partial ? half * 128 : col_h;
+        if (partial || (half_ok && wrow0 < p.M)) {
           // formed here rather than hoisted out of the tile loop, so that they
           // hold no registers during the K loop
-          uint32_t wl = (warp << 8) | lane;
-          asm volatile("" : "+r"(wl));
-          const uint32_t cbuf = smem_u32(sm.cst[0]) + (wl >> 8) * CST_BYTES;
-          const uint32_t srow = cbuf + (wl & 31) * CST_ROW;
-          const uint32_t swz = ((wl & 31) >> 1) & 3;
-          const int W = p.c_f32 ? 16 : 32;        // columns per chunk
+          uint32_t wl_ = (warp << 8) | lane;
+          asm volatile("" : "+r"(wl_));
+          const uint32_t cbuf = smem_u32(sm.cst[0]) + (wl_ >> 8) * CST_BYTES;
+          const uint32_t srow = cbuf + (wl_ & 31) * CST_ROW;
+          const uint32_t swz = ((wl_ & 31) >> 1) & 3;
+          const int W = f32 ? 16 : 32;             // columns per chunk
 #pragma unroll
           for (int q = 0; q < 8; ++q) {
-            if ((p.c_f32 || q < 4) && col_h + q * W < p.N) {
+            if ((f32 || q < 4) && (partial || col_h + q * W < p.N)) {
               if (staged) {
                 if (lane == 0) bulk_wait_read_all();
                 __syncwarp();
@@ -796,7 +883,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
               for (int u = 0; u < 4; ++u) {
                 uint32_t w[4];
-                if (p.c_f32) {
+                if (f32) {
                   // columns 16q + 4u .. +3 = accumulator pairs 8q + 2u, +1
                   const uint64_t x0 = acc[8 * q + 2 * u], x1 = acc[8 * q + 2 * u + 1];
                   w[0] = static_cast<uint32_t>(x0);
@@ -818,7 +905,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
               fence_proxy_async_smem();
               __syncwarp();
               if (lane == 0) {
-                tma_store_2d(&tmC, cbuf, col_h + q * W, wrow0);
+                tma_store_2d(partial ? &tmW : &tmC, cbuf, wcol0 + q * W, wrow0);
                 bulk_commit();
               }
               staged = true;
@@ -836,6 +923,59 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   if (warp == MMA_WARP) {
     tc_fence_after();
     tmem_dealloc(tmem_base, TMEM_COLS);
+  }
+}
+
+// Stream-K fix-up: one CTA per stream-K tile.  The CTAs that worked on the
+// tile are found from the same even split of the slices as in WorkList (CTAs
+// whose share is empty, when there are fewer slices than CTAs, are skipped); a
+// tile one CTA finished was stored by it and is skipped.  Otherwise the CTAs'
+// partial sums are added in CTA order (FP32, so the result does not depend on
+// timing) and the tile is written to C, clipped at M and N.
+constexpr int kFixupRowsPerCta = 16;     // a tile's fix-up is spread over BM / 16 CTAs
+
+template <bool F32OUT>
+__global__ void __launch_bounds__(256) streamk_fixup_kernel(const float* __restrict__ ws,
+                                                            void* __restrict__ c, const GemmParams p) {
+  const int j = blockIdx.x;
+  const long long S = p.sk_iters;
+  const long long G = p.sk_grid;
+  const long long x0 = static_cast<long long>(j) * p.nkb, x1 = x0 + p.nkb;
+  auto lo_of = [&](long long b) { return S * b / G; };
+  auto cta_of = [&](long long x) {
+    long long b = x * G / S;
+    while (lo_of(b + 1) <= x) ++b;
+    return b;
+  };
+  const long long b0 = cta_of(x0), b1 = cta_of(x1 - 1);
+  if (b0 == b1) return;
+  const Tile tl = dense_tile(p.dp_tiles + j, p);
+  const int cg = (threadIdx.x & 63) * 4;             // four columns of the tile
+  const int r0 = blockIdx.y * kFixupRowsPerCta;
+  for (int r = r0 + (threadIdx.x >> 6); r < r0 + kFixupRowsPerCta; r += 4) {
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (long long b = b0; b <= b1; ++b) {
+      if (lo_of(b + 1) == lo_of(b)) continue;         // a CTA with no slices wrote nothing
+      const int slot = lo_of(b) >= x0 ? 0 : 1;
+      const float4 v = __ldg(reinterpret_cast<const float4*>(
+          ws + ((b * 2 + slot) * BM + r) * static_cast<long long>(BN) + cg));
+      acc.x = __fadd_rn(acc.x, v.x);
+      acc.y = __fadd_rn(acc.y, v.y);
+      acc.z = __fadd_rn(acc.z, v.z);
+      acc.w = __fadd_rn(acc.w, v.w);
+    }
+    const int row = tl.m0 + r, col = tl.n0 + cg;
+    if (row >= p.M || col >= p.N) continue;           // N % 16 == 0: four columns are in or out together
+    if constexpr (F32OUT) {
+      *reinterpret_cast<float4*>(static_cast<float*>(c) + static_cast<long long>(row) * p.N + col) = acc;
+    } else {
+      const __nv_bfloat162 lo2 = __floats2bfloat162_rn(acc.x, acc.y);
+      const __nv_bfloat162 hi2 = __floats2bfloat162_rn(acc.z, acc.w);
+      uint2 v;
+      v.x = *reinterpret_cast<const uint32_t*>(&lo2);
+      v.y = *reinterpret_cast<const uint32_t*>(&hi2);
+      *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(c) + static_cast<long long>(row) * p.N + col) = v;
+    }
   }
 }
 
@@ -903,10 +1043,66 @@ cudaError_t set_smem_attr() {
 
 }  // namespace
 
+namespace {
+
+// Stream-K plan of a dense launch (see WorkList): tiles [0, dp_tiles) whole,
+// the slices of the rest split evenly over `grid` CTAs.  Used when the last
+// wave of whole tiles would leave at least kStreamKMinSlices slice-steps of
+// most SMs idle (or when forced), and never in the whole-K study mode.
+constexpr int kStreamKMinSlices = 40;
+
+struct SplitPlan {
+  int grid;
+  int dp_tiles;
+  long long sk_iters;
+};
+
+SplitPlan plan_split(int64_t tiles, int nkb, int sms, bool allow, bool force) {
+  SplitPlan s{static_cast<int>(tiles < sms ? tiles : sms), INT32_MAX, 0};
+  if (!allow || sms <= 0) return s;
+  const int64_t rem = tiles % sms;
+  if (rem == 0 && !force) return s;
+  const int64_t idle_slices = (sms - rem) * static_cast<int64_t>(nkb) / sms;   // per SM, last wave
+  if (!force && idle_slices < kStreamKMinSlices) return s;
+  // the full waves stay whole tiles; only the leftover tiles' slices are spread
+  // over all SMs (one partial store per SM at most, measured faster than also
+  // spreading the last full wave)
+  const int64_t dp = (tiles / sms) * sms;
+  const int64_t iters = (tiles - dp) * static_cast<int64_t>(nkb);
+  if (iters >= (int64_t{1} << 31)) return s;
+  s.grid = sms;
+  s.dp_tiles = static_cast<int>(dp);
+  s.sk_iters = iters;
+  return s;
+}
+
+}  // namespace
+
+size_t gemm_workspace_bytes(int64_t M, int64_t N, int64_t K, bool whole_k, bool force_sk) {
+  const int64_t tiles = ((M + BM - 1) / BM) * ((N + BN - 1) / BN);
+  const SplitPlan s = plan_split(tiles, static_cast<int>(K / BK), device_sm_count(), !whole_k, force_sk);
+  if (s.sk_iters == 0) return 0;
+  return static_cast<size_t>(s.grid) * 2 * BM * BN * sizeof(float);
+}
+
+namespace {
+
+// FP32 partial tiles of the stream-K workspace, [grid * 2 * BM rows, BN], stored
+// like an FP32 C by 32-row x 64-byte boxes from 64-byte-swizzled staging.
+bool make_ws_map(CUtensorMap* mW, float* ws, int grid) {
+  const uint64_t dW[2] = {static_cast<uint64_t>(BN), static_cast<uint64_t>(grid) * 2 * BM};
+  const uint64_t sW[1] = {static_cast<uint64_t>(BN) * 4};
+  const uint32_t boxW[2] = {static_cast<uint32_t>(CST_ROW / 4), 32};
+  return encode_tensor_map(mW, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, ws, 2, dW, sW, boxW,
+                           CU_TENSOR_MAP_SWIZZLE_64B);
+}
+
+}  // namespace
+
 fp8fg_status launch_gemm(const uint8_t* a, const float* sa, const uint8_t* b, const float* sb,
                          void* c, fp8fg_dtype ct, int64_t M, int64_t N, int64_t K, bool b_tile,
-                         bool whole_k, cudaStream_t st) {
-  CUtensorMap mA, mB, mC;
+                         bool whole_k, void* ws, size_t ws_bytes, bool force_sk, cudaStream_t st) {
+  CUtensorMap mA, mB, mC, mW;
   if (!make_maps(&mA, &mB, a, M, b, 0, N, K) || !make_c_map(&mC, c, ct, M, N))
     return FP8FG_ERR_CUDA;
   if ((b_tile ? set_smem_attr<false, true>()
@@ -930,16 +1126,40 @@ fp8fg_status launch_gemm(const uint8_t* a, const float* sa, const uint8_t* b, co
   p.b_tile = b_tile ? 1 : 0;
   p.wait_limit = wait_limit_cycles();
   p.status = device_status_word();
-  const int tiles = p.m_tiles * p.n_tiles;
-  const int grid = tiles < device_sm_count() ? tiles : device_sm_count();
+  const int64_t tiles = static_cast<int64_t>(p.m_tiles) * p.n_tiles;
+  // stream-K only with a workspace large enough for this device's split
+  const size_t need = gemm_workspace_bytes(M, N, K, whole_k, force_sk);
+  const bool sk = ws != nullptr && need > 0 && ws_bytes >= need;
+  const SplitPlan plan = plan_split(tiles, p.nkb, device_sm_count(), sk, force_sk);
+  p.dp_tiles = plan.dp_tiles;
+  p.sk_iters = plan.sk_iters;
+  p.sk_grid = plan.grid;
+  if (plan.sk_iters > 0) {
+    if (!make_ws_map(&mW, static_cast<float*>(ws), plan.grid)) return FP8FG_ERR_CUDA;
+  } else {
+    mW = mC;                         // unused
+  }
+  const int grid = plan.grid;
   if (b_tile)
-    blockscaled_gemm_kernel<false, true, EPI_STORE><<<grid, NUM_THREADS, smem_bytes<false, true>(), st>>>(mA, mB, mC, p);
+    blockscaled_gemm_kernel<false, true, EPI_STORE>
+        <<<grid, NUM_THREADS, smem_bytes<false, true>(), st>>>(mA, mB, mC, mW, p);
   else if (whole_k)
-    blockscaled_gemm_kernel<false, false, EPI_WHOLEK><<<grid, NUM_THREADS, smem_bytes<false, false>(), st>>>(mA, mB, mC,
-                                                                                           p);
+    blockscaled_gemm_kernel<false, false, EPI_WHOLEK>
+        <<<grid, NUM_THREADS, smem_bytes<false, false>(), st>>>(mA, mB, mC, mW, p);
   else
-    blockscaled_gemm_kernel<false, false, EPI_STORE><<<grid, NUM_THREADS, smem_bytes<false, false>(), st>>>(mA, mB, mC, p);
-  return cudaGetLastError() == cudaSuccess ? FP8FG_OK : FP8FG_ERR_CUDA;
+    blockscaled_gemm_kernel<false, false, EPI_STORE>
+        <<<grid, NUM_THREADS, smem_bytes<false, false>(), st>>>(mA, mB, mC, mW, p);
+  if (cudaGetLastError() != cudaSuccess) return FP8FG_ERR_CUDA;
+  if (plan.sk_iters > 0) {
+    const int sk_tiles = static_cast<int>(plan.sk_iters / p.nkb);
+    const dim3 fgrid(static_cast<unsigned>(sk_tiles), BM / kFixupRowsPerCta);
+    if (p.c_f32)
+      streamk_fixup_kernel<true><<<fgrid, 256, 0, st>>>(static_cast<const float*>(ws), c, p);
+    else
+      streamk_fixup_kernel<false><<<fgrid, 256, 0, st>>>(static_cast<const float*>(ws), c, p);
+    if (cudaGetLastError() != cudaSuccess) return FP8FG_ERR_CUDA;
+  }
+  return FP8FG_OK;
 }
 
 fp8fg_status launch_gemm_quant(const uint8_t* a, const float* sa, const uint8_t* b,
@@ -979,9 +1199,9 @@ fp8fg_status launch_gemm_quant(const uint8_t* a, const float* sa, const uint8_t*
   const int tiles = p.m_tiles * p.n_tiles;
   const int grid = tiles < device_sm_count() ? tiles : device_sm_count();
   if (b_tile)
-    blockscaled_gemm_kernel<false, true, EPI_QUANT><<<grid, NUM_THREADS, smem_bytes<false, true>(), st>>>(mA, mB, mQ, p);
+    blockscaled_gemm_kernel<false, true, EPI_QUANT><<<grid, NUM_THREADS, smem_bytes<false, true>(), st>>>(mA, mB, mQ, mQ, p);
   else
-    blockscaled_gemm_kernel<false, false, EPI_QUANT><<<grid, NUM_THREADS, smem_bytes<false, false>(), st>>>(mA, mB, mQ, p);
+    blockscaled_gemm_kernel<false, false, EPI_QUANT><<<grid, NUM_THREADS, smem_bytes<false, false>(), st>>>(mA, mB, mQ, mQ, p);
   return cudaGetLastError() == cudaSuccess ? FP8FG_OK : FP8FG_ERR_CUDA;
 }
 
@@ -1011,7 +1231,7 @@ fp8fg_status launch_grouped_gemm(const uint8_t* a, const float* sa, const int32_
   p.wait_limit = wait_limit_cycles();
   p.status = device_status_word();
   blockscaled_gemm_kernel<true, false, EPI_STORE><<<device_sm_count(), NUM_THREADS, smem_bytes<true, false>(), st>>>(
-      mA, mB, mC, p);
+      mA, mB, mC, mC, p);
   return cudaGetLastError() == cudaSuccess ? FP8FG_OK : FP8FG_ERR_CUDA;
 }
 
@@ -1060,7 +1280,7 @@ fp8fg_status launch_grouped_swiglu_quant(const uint8_t* a, const float* sa,
                          CU_TENSOR_MAP_SWIZZLE_64B))
     return FP8FG_ERR_CUDA;
   blockscaled_gemm_kernel<true, false, EPI_SWIGLU><<<device_sm_count(), NUM_THREADS, smem_bytes<true, false>(),
-                                                     st>>>(mA, mB, mQ, p);
+                                                     st>>>(mA, mB, mQ, mQ, p);
   return cudaGetLastError() == cudaSuccess ? FP8FG_OK : FP8FG_ERR_CUDA;
 }
 

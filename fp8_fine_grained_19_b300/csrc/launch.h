@@ -34,9 +34,13 @@ cudaError_t launch_weight_quant(const void* w, fp8fg_dtype wt, int64_t N, int64_
 
 // Dense block-scaled GEMM (b_tile: B carries 1x128 tile scales).
 // whole_k: study mode, all of K accumulated in the tensor core, per-tensor scales.
+// ws / ws_bytes: optional stream-K workspace (used when at least
+// gemm_workspace_bytes(...) bytes); force_sk splits even when it would not pay.
 fp8fg_status launch_gemm(const uint8_t* a, const float* sa, const uint8_t* b, const float* sb,
                          void* c, fp8fg_dtype ct, int64_t M, int64_t N, int64_t K, bool b_tile,
-                         bool whole_k, cudaStream_t st);
+                         bool whole_k, void* ws, size_t ws_bytes, bool force_sk, cudaStream_t st);
+// Workspace a stream-K split of this dense GEMM needs on the current device (0: not split).
+size_t gemm_workspace_bytes(int64_t M, int64_t N, int64_t K, bool whole_k, bool force_sk);
 // Dense block-scaled GEMM whose result leaves as 1x128 E4M3 tiles (q, s).
 fp8fg_status launch_gemm_quant(const uint8_t* a, const float* sa, const uint8_t* b,
                                const float* sb, uint8_t* q, float* s, int64_t M, int64_t N,

@@ -31,6 +31,7 @@
 #ifndef FP8FG_H_
 #define FP8FG_H_
 
+#include <stddef.h>
 #include <stdint.h>
 
 #ifdef __cplusplus
@@ -54,6 +55,8 @@ typedef enum { FP8FG_BF16 = 0, FP8FG_F32 = 1 } fp8fg_dtype;
 #define FP8FG_TRANSPOSE 2u     /* act_quant: 128x1 tiles, transposed output */
 #define FP8FG_B_TILE1x128 4u   /* GEMM: B carries 1x128 tile scales [N, K/128] */
 #define FP8FG_WHOLE_K 8u       /* GEMM study mode: no per-128-K promotion (see below) */
+#define FP8FG_STREAM_K 16u     /* fp8_blockscaled_gemm_ws: split the K slices even when it
+                                  would not pay (tests, studies) */
 
 /*
  * fp8_act_quant -- online 1x128 tile quantisation of activations to E4M3.
@@ -139,6 +142,41 @@ fp8fg_status fp8_weight_quant(const void* w, fp8fg_dtype w_dtype, int64_t N, int
 fp8fg_status fp8_blockscaled_gemm(const uint8_t* a, const float* sa, const uint8_t* b,
                                   const float* sb, void* c, fp8fg_dtype c_dtype, int64_t M,
                                   int64_t N, int64_t K, unsigned flags, void* stream);
+
+/*
+ * fp8_blockscaled_gemm_ws -- fp8_blockscaled_gemm with a caller-owned workspace
+ * for a stream-K split of the work.  Same operation, arguments and rules as
+ * fp8_blockscaled_gemm (page 2, promotion passage and Figure 6); flags within
+ * FP8FG_B_TILE1x128 | FP8FG_STREAM_K.
+ *
+ * When the last wave of whole 128x256 output tiles would leave most SMs idle
+ * for at least 40 of the 128-K slices (the Dgrad shape 4096 x 7168 x 18432: 896
+ * tiles on 148 SMs), the first waves run as whole tiles and the slices of the
+ * remaining tiles are divided evenly among all SMs; a tile whose slices fall
+ * to several SMs is summed in FP32 from their partial sums, in a fixed order,
+ * by a second kernel on the same stream (same result for every run; one to
+ * two more FP32 additions per element than the whole-tile path).
+ * FP8FG_STREAM_K applies the split whenever the tiles do not fill whole waves.
+ *
+ * workspace  DEVICE, 16-byte aligned, at least
+ *            fp8_blockscaled_gemm_workspace_bytes(M, N, K, flags) bytes (the
+ *            split needs 256 KB per SM of the current device: 37 MB on 148
+ *            SMs), or NULL: then no split is made (FP8FG_STREAM_K then fails
+ *            with FP8FG_ERR_INVALID_ARG).  Its contents on entry do not matter;
+ *            it must not be used by another call running at the same time.
+ * A non-NULL workspace smaller than needed: FP8FG_ERR_INVALID_ARG.
+ */
+fp8fg_status fp8_blockscaled_gemm_ws(const uint8_t* a, const float* sa, const uint8_t* b,
+                                     const float* sb, void* c, fp8fg_dtype c_dtype, int64_t M,
+                                     int64_t N, int64_t K, unsigned flags, void* workspace,
+                                     size_t workspace_bytes, void* stream);
+
+/*
+ * fp8_blockscaled_gemm_workspace_bytes -- workspace bytes fp8_blockscaled_gemm_ws
+ * uses for this shape and flags on the current device; 0 when it would not
+ * split the work (or without a device, or for invalid sizes).
+ */
+size_t fp8_blockscaled_gemm_workspace_bytes(int64_t M, int64_t N, int64_t K, unsigned flags);
 
 /*
  * fp8_blockscaled_gemm_quant -- fp8_blockscaled_gemm whose FP32 result is

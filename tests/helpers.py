@@ -138,7 +138,7 @@ def check_quant_decisions(q_gpu, s_gpu, x_ref, err, pow2):
     return float(sure.mean())
 
 
-def gemm_error_bound(qa, sa, qb, sb, b_tile=False) -> np.ndarray:
+def gemm_error_bound(qa, sa, qb, sb, b_tile=False, extra_adds=0) -> np.ndarray:
     """Per-element bound on |C32 - C| for the promoted FP32 sum (float64 [M, N]).
 
     C = sum_kb P_kb * s_kb is the oracle's exact result (s_kb = sa[m,kb] * sb(n,kb)).
@@ -158,6 +158,10 @@ def gemm_error_bound(qa, sa, qb, sb, b_tile=False) -> np.ndarray:
     Hence |C32 - C| <= (nkb + 1) 2^-24 A1 + 8 * 2^-24 A2 (second-order terms are
     far below the first-order slack).  A single wrong element (a dropped group, a
     wrong scale) misses it by orders of magnitude.
+
+    extra_adds: FP32 additions of partial sums beyond the per-group ones (a tile
+    whose groups were split among CTAs is summed from its parts: one addition per
+    extra part, each within 2^-24 of a magnitude bounded by A1).
     """
     qa = np.asarray(qa)
     qb = np.asarray(qb)
@@ -177,7 +181,7 @@ def gemm_error_bound(qa, sa, qb, sb, b_tile=False) -> np.ndarray:
         s = sa64[:, kb][:, None] * sbk[None, :]
         A1 += np.abs(P) * s
         A2 += Q * s
-    return (nkb + 1) * 2.0 ** -24 * A1 + 8 * 2.0 ** -24 * A2
+    return (nkb + 1 + extra_adds) * 2.0 ** -24 * A1 + 8 * 2.0 ** -24 * A2
 
 
 def grouped_error_bound(qa, sa, offsets, qb, sb) -> np.ndarray:

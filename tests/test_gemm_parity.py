@@ -143,7 +143,13 @@ def test_dgrad_wgrad_full_size(cuda_lib):
     rows = _sample_rows(4096, 24, 3)
     ref = H.oracle_gemm_chunked(qd_r[rows], sd_r[rows], qwt_r, swt_r)
     assert H.normwise_rel_err(dx[rows], ref) <= TOL[torch.bfloat16]
-    H.assert_elementwise(dx[rows], ref, H.gemm_error_bound(qd_r[rows], sd_r[rows], qwt_r, swt_r),
+    # this shape leaves most SMs idle in its last wave of whole tiles, so the
+    # binding spreads the 128-K groups of the leftover tiles over all SMs
+    # (stream-K): a split tile is summed from its parts, at most one FP32
+    # addition per group beyond the whole-tile path
+    H.assert_elementwise(dx[rows], ref,
+                         H.gemm_error_bound(qd_r[rows], sd_r[rows], qwt_r, swt_r,
+                                            extra_adds=qd_r.shape[1] // 128),
                          "dgrad")
     # Wgrad: A = dY^T (128x1 tiles along tokens), B = X^T (128x1 tiles), tile x tile scales
     qdt, sdt = cuda_lib.act_quant(dy.cuda(), transpose=True)

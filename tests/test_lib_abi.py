@@ -40,7 +40,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_abi_version_and_status_strings(lib):
-    assert lib.fp8fg_abi_version() == 5
+    assert lib.fp8fg_abi_version() == 6
     for code in range(7):
         assert fp8.status_string(code)
     assert "unknown" in fp8.status_string(99)
@@ -163,3 +163,24 @@ def test_binding_rejects_mixed_devices():
     with pytest.raises(ValueError):
         fp8._same_device(a, b)
     assert fp8._same_device(a, None, a) == a.device
+
+
+def test_gemm_ws_rejections(lib):
+    f = lib.fp8_blockscaled_gemm_ws
+    ok = (A16, A16, A16, A16, A16)
+    st = fp8.STREAM_K
+    assert f(*ok, 0, 128, 256, 256, fp8.WHOLE_K, A16, 1 << 30, None) == fp8.ERR_INVALID_ARG   # no study mode
+    assert f(*ok, 0, 128, 256, 256, 32, A16, 1 << 30, None) == fp8.ERR_INVALID_ARG            # unknown flag
+    assert f(*ok, 0, 128, 256, 256, st, None, 0, None) == fp8.ERR_INVALID_ARG                 # forced, no workspace
+    assert f(*ok, 0, 128, 256, 200, 0, A16, 1 << 30, None) == fp8.ERR_UNSUPPORTED_SHAPE       # K % 128
+    assert f(*ok, 0, 128, 256, 256, 0, MIS, 1 << 30, None) == fp8.ERR_MISALIGNED              # workspace
+    assert f(None, None, A16, A16, None, 0, 0, 256, 256, st, A16, 1 << 30, None) == fp8.OK    # M == 0
+    # the plain entry point has no workspace, so it rejects the forced split
+    assert lib.fp8_blockscaled_gemm(*ok, 0, 128, 256, 256, st, None) == fp8.ERR_INVALID_ARG
+
+
+def test_workspace_query_without_device(lib):
+    # without a device (or for invalid sizes) nothing is split
+    assert lib.fp8_blockscaled_gemm_workspace_bytes(4096, 7168, 18432, 0) in (0, 148 * 2 * 128 * 256 * 4)
+    assert lib.fp8_blockscaled_gemm_workspace_bytes(0, 7168, 18432, 0) == 0
+    assert lib.fp8_blockscaled_gemm_workspace_bytes(128, 256, 200, 0) == 0

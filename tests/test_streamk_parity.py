@@ -1,0 +1,94 @@
+"""Stream-K split of the dense block-scaled GEMM vs the oracle and vs the whole-tile path.
+
+fp8_blockscaled_gemm_ws divides the 128-K groups of the last output tiles evenly
+among all SMs; a tile whose groups fall to several CTAs is summed from their FP32
+partial sums by a second kernel, in a fixed order.  The result is the promoted
+sum of page 2 (inprokorea.com free #735329, promotion passage and Figure 6) with
+one more FP32 addition per extra part, so the per-element bound gains that many
+terms (tests/helpers.py, gemm_error_bound, extra_adds).  Forced splits on small
+ragged shapes put up to one group per CTA, so a tile may have as many parts as
+groups; the Dgrad shape (896 tiles on 148 SMs) splits on its own.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from oracle import e4m3
+from tests import helpers as H
+
+pytestmark = pytest.mark.gpu
+
+TOL = {torch.float32: 1e-5, torch.bfloat16: 4e-3}
+
+
+def _operands(M, N, K, seed, b_tile=False):
+    g = np.random.default_rng(seed)
+    qa = e4m3.encode((g.standard_normal((M, K)) * 60).astype(np.float32))
+    qb = e4m3.encode((g.standard_normal((N, K)) * 60).astype(np.float32))
+    sa = np.exp(g.uniform(-4, 4, (M, K // 128))).astype(np.float32)
+    sb = np.exp(g.uniform(-4, 4, (N, K // 128) if b_tile else (N // 128, K // 128))).astype(np.float32)
+    return qa, sa, qb, sb
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+@pytest.mark.parametrize("M,N,K,b_tile", [(300, 768, 1280, False), (129, 400, 2048, True),
+                                          (1, 128, 6144, False), (520, 1024, 384, False),
+                                          (700, 2304, 1024, True)])
+def test_forced_split_vs_oracle(cuda_lib, M, N, K, b_tile, dtype):
+    qa, sa, qb, sb = _operands(M, N, K, M + 3 * N + K, b_tile)
+    assert cuda_lib.gemm_workspace_bytes(M, N, K, b_tile, stream_k=True) > 0
+    d = [H.to_dev(v) for v in (qa, sa, qb, sb)]
+    raw, out = H.guarded_empty((M, N), dtype)
+    cuda_lib.gemm(*d, b_tile=b_tile, out=out, stream_k=True)
+    torch.cuda.synchronize()
+    assert cuda_lib.device_status() == cuda_lib.OK
+    assert H.guards_intact(raw), "write outside the output"
+    ref = oracle.gemm(qa, sa, qb, sb, b_tile=b_tile)
+    assert H.normwise_rel_err(out, ref) <= TOL[dtype]
+    nkb = K // 128
+    H.assert_elementwise(out, ref, H.gemm_error_bound(qa, sa, qb, sb, b_tile, extra_adds=nkb),
+                         f"stream-K {M}x{N}x{K}")
+    # the same result on every run (the parts are added in a fixed order)
+    again = cuda_lib.gemm(*d, b_tile=b_tile, out_dtype=dtype, stream_k=True)
+    assert torch.equal(out, again)
+    # and the whole-tile path agrees within both bounds
+    whole = cuda_lib.gemm(*d, b_tile=b_tile, out_dtype=dtype, stream_k=False)
+    H.assert_elementwise(whole, ref, H.gemm_error_bound(qa, sa, qb, sb, b_tile), "whole tiles")
+
+
+def test_split_with_caller_workspace_and_reuse(cuda_lib):
+    # a caller-owned workspace, reused by two different shapes in a row: its
+    # contents on entry do not matter
+    M, N, K = 300, 768, 1280
+    qa, sa, qb, sb = _operands(M, N, K, 5)
+    need = cuda_lib.gemm_workspace_bytes(M, N, K, stream_k=True)
+    ws = torch.full((need,), 0x7F, dtype=torch.uint8, device="cuda")
+    d = [H.to_dev(v) for v in (qa, sa, qb, sb)]
+    a = cuda_lib.gemm(*d, out_dtype=torch.float32, stream_k=True, workspace=ws)
+    qa2, sa2, qb2, sb2 = _operands(129, 384, 2048, 6, True)
+    cuda_lib.gemm(*[H.to_dev(v) for v in (qa2, sa2, qb2, sb2)], b_tile=True, out_dtype=torch.float32,
+                  stream_k=True, workspace=ws)
+    b = cuda_lib.gemm(*d, out_dtype=torch.float32, stream_k=True, workspace=ws)
+    assert torch.equal(a, b)
+    ref = oracle.gemm(qa, sa, qb, sb)
+    H.assert_elementwise(b, ref, H.gemm_error_bound(qa, sa, qb, sb, extra_adds=K // 128), "reuse")
+
+
+def test_workspace_too_small_is_rejected(cuda_lib):
+    M, N, K = 300, 768, 1280
+    qa, sa, qb, sb = [H.to_dev(v) for v in _operands(M, N, K, 7)]
+    need = cuda_lib.gemm_workspace_bytes(M, N, K, stream_k=True)
+    small = torch.empty(need - 16, dtype=torch.uint8, device="cuda")
+    with pytest.raises(cuda_lib.Fp8Error) as e:
+        cuda_lib.gemm(qa, sa, qb, sb, stream_k=True, workspace=small)
+    assert e.value.status == cuda_lib.ERR_INVALID_ARG
+
+
+def test_auto_split_on_the_dgrad_shape(cuda_lib):
+    # 896 output tiles on the SMs: the last wave would leave most SMs idle for
+    # most of the 144 groups, so the automatic choice splits
+    assert cuda_lib.gemm_workspace_bytes(4096, 7168, 18432) > 0
+    # the Fprop shape's last wave is nearly full: no split
+    assert cuda_lib.gemm_workspace_bytes(4096, 18432, 7168) == 0
