@@ -122,39 +122,44 @@ struct GemmParams {
   long long wait_limit;
   int* status;            // library status word
   // Work split (see WorkList): tiles [0, dp_tiles) are whole tiles taken
-  // round-robin; the 128-K slices of the tiles after them (sk_iters slices in
-  // all) are divided evenly among the CTAs (stream-K).  A tile whose slices
-  // fall to more than one CTA leaves FP32 partial sums in the workspace ws
-  // ([grid][2][BM][BN]); the fix-up kernel adds them up.
+  // round-robin; each of the sk_tiles tiles after them is shared by its own
+  // group of CTAs, which divide its 128-K slices evenly (stream-K).  A tile
+  // shared by several CTAs leaves FP32 partial sums in the workspace
+  // ([sk_grid][BM][BN], one slot per CTA); the fix-up kernel adds them up.
   int dp_tiles = INT32_MAX;
-  long long sk_iters = 0;
-  int sk_grid = 0;        // grid size of the stream-K launch (the fix-up recomputes the split)
+  int sk_tiles = 0;
+  int sk_grid = 0;        // CTAs taking part in the split (the fix-up recomputes it)
 };
 
 // One unit of a CTA's work: slices [kb0, kb1) of tile t.  slot -1: the whole
-// tile (its result goes to C); 0 or 1: a part of a tile split between CTAs,
-// whose partial sum goes to the CTA's workspace slot (0: the first unit of
-// its stream-K range, 1: the last).
+// tile (its result goes to C); 0: a part of a tile shared between CTAs, whose
+// partial sum goes to the CTA's workspace slot.
 struct Work {
   int t, kb0, kb1, slot;
 };
 
+// The stream-K group of CTAs sharing split tile j (R = sk_tiles <= G = sk_grid
+// CTAs): CTAs [first(j), first(j + 1)) with first(j) = ceil(j G / R); CTA b
+// belongs to tile floor(b R / G).
+__host__ __device__ __forceinline__ int sk_first_cta(int j, int R, int G) {
+  return static_cast<int>((static_cast<long long>(j) * G + R - 1) / R);
+}
+// Slices [kb0, kb1) of its tile that member i of a group of n CTAs takes.
+__host__ __device__ __forceinline__ void sk_share(int i, int n, int nkb, int& kb0, int& kb1) {
+  kb0 = static_cast<int>(static_cast<long long>(i) * nkb / n);
+  kb1 = static_cast<int>(static_cast<long long>(i + 1) * nkb / n);
+}
+
 // The sequence of units of this CTA, the same for every warp role.  Only the
-// dense kernels that store C (SK) split slices; the others take whole tiles
-// round-robin.  Slice positions are 32-bit (the host splits only when the
-// stream-K slices number fewer than 2^31).
+// dense kernels that store C (SK) split tiles; the others take whole tiles
+// round-robin.
 template <bool SK>
 struct WorkList {
-  int next_dp, x, lo, hi;
+  int next_dp;
+  bool sk_pending;
   __device__ __forceinline__ void init(const GemmParams& p) {
     next_dp = blockIdx.x;
-    if constexpr (SK) {
-      lo = static_cast<int>(p.sk_iters * blockIdx.x / gridDim.x);
-      hi = static_cast<int>(p.sk_iters * (blockIdx.x + 1) / gridDim.x);
-    } else {
-      lo = hi = 0;
-    }
-    x = lo;
+    sk_pending = SK && static_cast<int>(blockIdx.x) < p.sk_grid && p.sk_tiles > 0;
   }
   __device__ __forceinline__ bool next(const GemmParams& p, int num_tiles, Work& w) {
     if (next_dp < min(p.dp_tiles, num_tiles)) {
@@ -165,15 +170,15 @@ struct WorkList {
     if constexpr (!SK) {
       return false;
     } else {
-      if (x >= hi) return false;
-      const int j = x / p.nkb;
-      const int kb0 = x - j * p.nkb;
-      const int kb1 = hi - x < p.nkb - kb0 ? kb0 + (hi - x) : p.nkb;
-      w.t = p.dp_tiles + j;
-      w.kb0 = kb0;
-      w.kb1 = kb1;
-      w.slot = (kb0 == 0 && kb1 == p.nkb) ? -1 : (x == lo ? 0 : 1);
-      x += kb1 - kb0;
+      if (!sk_pending) return false;
+      sk_pending = false;
+      const int R = p.sk_tiles, G = p.sk_grid, b = blockIdx.x;
+      const int j = static_cast<int>(static_cast<long long>(b) * R / G);
+      const int f = sk_first_cta(j, R, G), n = sk_first_cta(j + 1, R, G) - f;
+      int kb0, kb1;
+      sk_share(b - f, n, p.nkb, kb0, kb1);
+      if (kb0 == kb1) return false;                 // more CTAs than slices in this group
+      w = {p.dp_tiles + j, kb0, kb1, n == 1 ? -1 : 0};
       return true;
     }
   }
@@ -313,7 +318,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
     tma_prefetch_desc(&tmC);
-    if (p.sk_iters > 0) tma_prefetch_desc(&tmW);
+    if (p.sk_tiles > 0) tma_prefetch_desc(&tmW);
   }
   if constexpr (GROUPED) {
     // Copy and check the offsets, then prefix the per-expert tile counts with
@@ -857,12 +862,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         // row `lane`, its 16-byte unit u at unit u ^ ((lane/2) % 4) (the 64-byte
         // swizzle), so a warp's st.shared.v4 hits every bank once per 8 lanes;
         // one TMA store writes the chunk and clips rows at or past M.  A part
-        // of a tile split between CTAs (stream-K) goes whole, in FP32, to this
+        // of a tile shared between CTAs (stream-K) goes whole, in FP32, to this
         // CTA's workspace slot instead, for the fix-up kernel to add up.
         const bool partial = wk.slot >= 0;
         const bool f32 = partial || p.c_f32;
-        const int wrow0 = partial ? (static_cast<int>(blockIdx.x) * 2 + wk.slot) * BM + quad * 32
-                                  : tl.m0 + quad * 32;
+        const int wrow0 = partial ? static_cast<int>(blockIdx.x) * BM + quad * 32 : tl.m0 + quad * 32;
         const int wcol0 = partial ? half * 128 : col_h;
         if (partial || (half_ok && wrow0 < p.M)) {
           // formed here rather than hoisted out of the tile loop, so that they
@@ -926,39 +930,32 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   }
 }
 
-// Stream-K fix-up: one CTA per stream-K tile.  The CTAs that worked on the
-// tile are found from the same even split of the slices as in WorkList (CTAs
-// whose share is empty, when there are fewer slices than CTAs, are skipped); a
-// tile one CTA finished was stored by it and is skipped.  Otherwise the CTAs'
-// partial sums are added in CTA order (FP32, so the result does not depend on
-// timing) and the tile is written to C, clipped at M and N.
-constexpr int kFixupRowsPerCta = 16;     // a tile's fix-up is spread over BM / 16 CTAs
+// Stream-K fix-up: BM / kFixupRowsPerCta CTAs per split tile.  The tile's
+// group of CTAs is recomputed from the same split as in WorkList (members whose
+// share is empty, when the group has more CTAs than slices, wrote nothing); a
+// tile with a single member was stored by it and is skipped.  Otherwise the
+// members' partial sums are added in CTA order (FP32, so the result does not
+// depend on timing) and the tile is written to C, clipped at M and N.
+constexpr int kFixupRowsPerCta = 16;
 
 template <bool F32OUT>
 __global__ void __launch_bounds__(256) streamk_fixup_kernel(const float* __restrict__ ws,
                                                             void* __restrict__ c, const GemmParams p) {
   const int j = blockIdx.x;
-  const long long S = p.sk_iters;
-  const long long G = p.sk_grid;
-  const long long x0 = static_cast<long long>(j) * p.nkb, x1 = x0 + p.nkb;
-  auto lo_of = [&](long long b) { return S * b / G; };
-  auto cta_of = [&](long long x) {
-    long long b = x * G / S;
-    while (lo_of(b + 1) <= x) ++b;
-    return b;
-  };
-  const long long b0 = cta_of(x0), b1 = cta_of(x1 - 1);
-  if (b0 == b1) return;
+  const int R = p.sk_tiles, G = p.sk_grid;
+  const int f = sk_first_cta(j, R, G), n = sk_first_cta(j + 1, R, G) - f;
+  if (n == 1) return;
   const Tile tl = dense_tile(p.dp_tiles + j, p);
   const int cg = (threadIdx.x & 63) * 4;             // four columns of the tile
   const int r0 = blockIdx.y * kFixupRowsPerCta;
   for (int r = r0 + (threadIdx.x >> 6); r < r0 + kFixupRowsPerCta; r += 4) {
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (long long b = b0; b <= b1; ++b) {
-      if (lo_of(b + 1) == lo_of(b)) continue;         // a CTA with no slices wrote nothing
-      const int slot = lo_of(b) >= x0 ? 0 : 1;
+    for (int i = 0; i < n; ++i) {
+      int kb0, kb1;
+      sk_share(i, n, p.nkb, kb0, kb1);
+      if (kb0 == kb1) continue;
       const float4 v = __ldg(reinterpret_cast<const float4*>(
-          ws + ((b * 2 + slot) * BM + r) * static_cast<long long>(BN) + cg));
+          ws + (static_cast<long long>(f + i) * BM + r) * BN + cg));
       acc.x = __fadd_rn(acc.x, v.x);
       acc.y = __fadd_rn(acc.y, v.y);
       acc.z = __fadd_rn(acc.z, v.z);
@@ -1054,25 +1051,21 @@ constexpr int kStreamKMinSlices = 40;
 struct SplitPlan {
   int grid;
   int dp_tiles;
-  long long sk_iters;
+  int sk_tiles;
 };
 
+// The full waves stay whole tiles; each leftover tile is shared by a group of
+// about sms / leftover CTAs (all tiles, when there are fewer tiles than SMs).
 SplitPlan plan_split(int64_t tiles, int nkb, int sms, bool allow, bool force) {
   SplitPlan s{static_cast<int>(tiles < sms ? tiles : sms), INT32_MAX, 0};
   if (!allow || sms <= 0) return s;
   const int64_t rem = tiles % sms;
-  if (rem == 0 && !force) return s;
+  if (rem == 0) return s;
   const int64_t idle_slices = (sms - rem) * static_cast<int64_t>(nkb) / sms;   // per SM, last wave
   if (!force && idle_slices < kStreamKMinSlices) return s;
-  // the full waves stay whole tiles; only the leftover tiles' slices are spread
-  // over all SMs (one partial store per SM at most, measured faster than also
-  // spreading the last full wave)
-  const int64_t dp = (tiles / sms) * sms;
-  const int64_t iters = (tiles - dp) * static_cast<int64_t>(nkb);
-  if (iters >= (int64_t{1} << 31)) return s;
   s.grid = sms;
-  s.dp_tiles = static_cast<int>(dp);
-  s.sk_iters = iters;
+  s.dp_tiles = static_cast<int>(tiles - rem);
+  s.sk_tiles = static_cast<int>(rem);
   return s;
 }
 
@@ -1081,16 +1074,16 @@ SplitPlan plan_split(int64_t tiles, int nkb, int sms, bool allow, bool force) {
 size_t gemm_workspace_bytes(int64_t M, int64_t N, int64_t K, bool whole_k, bool force_sk) {
   const int64_t tiles = ((M + BM - 1) / BM) * ((N + BN - 1) / BN);
   const SplitPlan s = plan_split(tiles, static_cast<int>(K / BK), device_sm_count(), !whole_k, force_sk);
-  if (s.sk_iters == 0) return 0;
-  return static_cast<size_t>(s.grid) * 2 * BM * BN * sizeof(float);
+  if (s.sk_tiles == 0) return 0;
+  return static_cast<size_t>(s.grid) * BM * BN * sizeof(float);
 }
 
 namespace {
 
-// FP32 partial tiles of the stream-K workspace, [grid * 2 * BM rows, BN], stored
+// FP32 partial tiles of the stream-K workspace, [grid * BM rows, BN], stored
 // like an FP32 C by 32-row x 64-byte boxes from 64-byte-swizzled staging.
 bool make_ws_map(CUtensorMap* mW, float* ws, int grid) {
-  const uint64_t dW[2] = {static_cast<uint64_t>(BN), static_cast<uint64_t>(grid) * 2 * BM};
+  const uint64_t dW[2] = {static_cast<uint64_t>(BN), static_cast<uint64_t>(grid) * BM};
   const uint64_t sW[1] = {static_cast<uint64_t>(BN) * 4};
   const uint32_t boxW[2] = {static_cast<uint32_t>(CST_ROW / 4), 32};
   return encode_tensor_map(mW, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, ws, 2, dW, sW, boxW,
@@ -1132,9 +1125,9 @@ fp8fg_status launch_gemm(const uint8_t* a, const float* sa, const uint8_t* b, co
   const bool sk = ws != nullptr && need > 0 && ws_bytes >= need;
   const SplitPlan plan = plan_split(tiles, p.nkb, device_sm_count(), sk, force_sk);
   p.dp_tiles = plan.dp_tiles;
-  p.sk_iters = plan.sk_iters;
+  p.sk_tiles = plan.sk_tiles;
   p.sk_grid = plan.grid;
-  if (plan.sk_iters > 0) {
+  if (plan.sk_tiles > 0) {
     if (!make_ws_map(&mW, static_cast<float*>(ws), plan.grid)) return FP8FG_ERR_CUDA;
   } else {
     mW = mC;                         // unused
@@ -1150,9 +1143,8 @@ fp8fg_status launch_gemm(const uint8_t* a, const float* sa, const uint8_t* b, co
     blockscaled_gemm_kernel<false, false, EPI_STORE>
         <<<grid, NUM_THREADS, smem_bytes<false, false>(), st>>>(mA, mB, mC, mW, p);
   if (cudaGetLastError() != cudaSuccess) return FP8FG_ERR_CUDA;
-  if (plan.sk_iters > 0) {
-    const int sk_tiles = static_cast<int>(plan.sk_iters / p.nkb);
-    const dim3 fgrid(static_cast<unsigned>(sk_tiles), BM / kFixupRowsPerCta);
+  if (plan.sk_tiles > 0) {
+    const dim3 fgrid(static_cast<unsigned>(plan.sk_tiles), BM / kFixupRowsPerCta);
     if (p.c_f32)
       streamk_fixup_kernel<true><<<fgrid, 256, 0, st>>>(static_cast<const float*>(ws), c, p);
     else

@@ -151,16 +151,16 @@ fp8fg_status fp8_blockscaled_gemm(const uint8_t* a, const float* sa, const uint8
  *
  * When the last wave of whole 128x256 output tiles would leave most SMs idle
  * for at least 40 of the 128-K slices (the Dgrad shape 4096 x 7168 x 18432: 896
- * tiles on 148 SMs), the first waves run as whole tiles and the slices of the
- * remaining tiles are divided evenly among all SMs; a tile whose slices fall
- * to several SMs is summed in FP32 from their partial sums, in a fixed order,
- * by a second kernel on the same stream (same result for every run; one to
- * two more FP32 additions per element than the whole-tile path).
+ * tiles on 148 SMs), the full waves run as whole tiles and each leftover tile
+ * is shared by its own group of SMs, which divide its 128-K slices evenly; a
+ * shared tile is summed in FP32 from the group's partial sums, in a fixed
+ * order, by a second kernel on the same stream (same result for every run;
+ * one more FP32 addition per extra part than the whole-tile path).
  * FP8FG_STREAM_K applies the split whenever the tiles do not fill whole waves.
  *
  * workspace  DEVICE, 16-byte aligned, at least
  *            fp8_blockscaled_gemm_workspace_bytes(M, N, K, flags) bytes (the
- *            split needs 256 KB per SM of the current device: 37 MB on 148
+ *            split needs 128 KB per SM of the current device: 18.5 MB on 148
  *            SMs), or NULL: then no split is made (FP8FG_STREAM_K then fails
  *            with FP8FG_ERR_INVALID_ARG).  Its contents on entry do not matter;
  *            it must not be used by another call running at the same time.

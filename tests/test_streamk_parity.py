@@ -1,8 +1,9 @@
 """Stream-K split of the dense block-scaled GEMM vs the oracle and vs the whole-tile path.
 
-fp8_blockscaled_gemm_ws divides the 128-K groups of the last output tiles evenly
-among all SMs; a tile whose groups fall to several CTAs is summed from their FP32
-partial sums by a second kernel, in a fixed order.  The result is the promoted
+fp8_blockscaled_gemm_ws keeps the full waves of output tiles whole and shares
+each leftover tile among its own group of CTAs, which divide its 128-K groups
+evenly; a shared tile is summed from the group's FP32 partial sums by a second
+kernel, in a fixed order.  The result is the promoted
 sum of page 2 (inprokorea.com free #735329, promotion passage and Figure 6) with
 one more FP32 addition per extra part, so the per-element bound gains that many
 terms (tests/helpers.py, gemm_error_bound, extra_adds).  Forced splits on small
