@@ -41,6 +41,8 @@ _SIGS = {
     "fp8_blockscaled_gemm_ws": [_vp, _vp, _vp, _vp, _vp, ctypes.c_int, _i64, _i64, _i64, _u32, _vp,
                                 ctypes.c_size_t, _vp],
     "fp8_blockscaled_gemm_workspace_bytes": [_i64, _i64, _i64, _u32],
+    "fp8_blockscaled_gemm_noalloc": [_vp, _vp, _vp, _vp, _vp, ctypes.c_int, _i64, _i64, _i64, _u32,
+                                     _vp],
     "fp8_blockscaled_gemm_quant": [_vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _u32, _vp],
     "fp8_grouped_gemm": [_vp, _vp, _vp, _i32, _i64, _vp, _vp, _vp, ctypes.c_int, _i64, _i64,
                          _u32, _vp],

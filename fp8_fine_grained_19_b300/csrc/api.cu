@@ -257,6 +257,18 @@ fp8fg_status fp8_blockscaled_gemm_ws(const uint8_t* a, const float* sa, const ui
                      workspace, workspace_bytes, force, as_stream(stream));
 }
 
+fp8fg_status fp8_blockscaled_gemm_noalloc(const uint8_t* a, const float* sa, const uint8_t* b,
+                                          const float* sb, void* c, fp8fg_dtype c_dtype, int64_t M,
+                                          int64_t N, int64_t K, unsigned flags, void* stream) {
+  const fp8fg_status chk = check_gemm_args(a, sa, b, sb, c, c_dtype, M, N, K, flags,
+                                           FP8FG_B_TILE1x128 | FP8FG_STREAM_K);
+  if (chk != FP8FG_OK) return chk;
+  if (M == 0) return FP8FG_OK;
+  if (!have_device()) return FP8FG_ERR_CUDA;
+  return launch_gemm_noalloc(a, sa, b, sb, c, c_dtype, M, N, K, (flags & FP8FG_B_TILE1x128) != 0,
+                             (flags & FP8FG_STREAM_K) != 0, as_stream(stream));
+}
+
 fp8fg_status fp8_blockscaled_gemm_quant(const uint8_t* a, const float* sa, const uint8_t* b,
                                         const float* sb, uint8_t* q, float* s, int64_t M,
                                         int64_t N, int64_t K, unsigned flags, void* stream) {

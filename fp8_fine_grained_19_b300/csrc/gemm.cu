@@ -1276,6 +1276,50 @@ fp8fg_status launch_grouped_swiglu_quant(const uint8_t* a, const float* sa,
   return cudaGetLastError() == cudaSuccess ? FP8FG_OK : FP8FG_ERR_CUDA;
 }
 
+// ---------------------------------------------------------------------------
+// Allocation-free variant of the stream-K GEMM.  Some callers cannot allocate
+// device memory when they call the GEMM (code that runs while a memory pool is
+// locked or being captured, allocators that must not be re-entered, embedded
+// runtimes with a fixed memory budget).  For them the split's partial tiles go
+// to this file-scope array instead of a caller workspace.  It holds the split
+// of up to kNoAllocMaxSms SMs (128 KB each, 20 MiB); every GPU that loads the
+// library keeps it until the process exits.
+constexpr int kNoAllocMaxSms = 160;
+constexpr size_t kNoAllocScratchBytes = static_cast<size_t>(kNoAllocMaxSms) * BM * BN * sizeof(float);
+static __device__ __align__(256) float g_noalloc_scratch[kNoAllocScratchBytes / sizeof(float)];
+
+namespace {
+
+// Device address of g_noalloc_scratch on the current device, looked up on the
+// first call on each device (host code cannot use the symbol itself: it names a
+// host-side stand-in, not device memory).
+float* noalloc_scratch_address() {
+  static std::atomic<float*> cache[kMaxDevices] = {};
+  const int d = current_device();
+  if (d < 0) return nullptr;
+  float* p = cache[d].load(std::memory_order_acquire);
+  if (p != nullptr) return p;
+  void* addr = nullptr;
+  if (cudaGetSymbolAddress(&addr, g_noalloc_scratch) != cudaSuccess || addr == nullptr)
+    return nullptr;
+  p = static_cast<float*>(addr);
+  cache[d].store(p, std::memory_order_release);
+  return p;
+}
+
+}  // namespace
+
+fp8fg_status launch_gemm_noalloc(const uint8_t* a, const float* sa, const uint8_t* b,
+                                 const float* sb, void* c, fp8fg_dtype ct, int64_t M, int64_t N,
+                                 int64_t K, bool b_tile, bool force_sk, cudaStream_t st) {
+  if (gemm_workspace_bytes(M, N, K, false, force_sk) > kNoAllocScratchBytes)
+    return FP8FG_ERR_UNSUPPORTED_SHAPE;      // the split on this device needs more than the array
+  float* scratch = noalloc_scratch_address();
+  if (scratch == nullptr) return FP8FG_ERR_CUDA;
+  return launch_gemm(a, sa, b, sb, c, ct, M, N, K, b_tile, false, scratch, kNoAllocScratchBytes,
+                     force_sk, st);
+}
+
 cudaError_t launch_wait_timeout_selftest(uint32_t limit_cycles, cudaStream_t st) {
   wait_timeout_selftest_kernel<<<1, 32, 0, st>>>(static_cast<long long>(limit_cycles),
                                                  device_status_word());

@@ -41,6 +41,11 @@ fp8fg_status launch_gemm(const uint8_t* a, const float* sa, const uint8_t* b, co
                          bool whole_k, void* ws, size_t ws_bytes, bool force_sk, cudaStream_t st);
 // Workspace a stream-K split of this dense GEMM needs on the current device (0: not split).
 size_t gemm_workspace_bytes(int64_t M, int64_t N, int64_t K, bool whole_k, bool force_sk);
+// launch_gemm with the split's partial tiles in the library's own device array
+// (no caller workspace); FP8FG_ERR_UNSUPPORTED_SHAPE when the split needs more.
+fp8fg_status launch_gemm_noalloc(const uint8_t* a, const float* sa, const uint8_t* b,
+                                 const float* sb, void* c, fp8fg_dtype ct, int64_t M, int64_t N,
+                                 int64_t K, bool b_tile, bool force_sk, cudaStream_t st);
 // Dense block-scaled GEMM whose result leaves as 1x128 E4M3 tiles (q, s).
 fp8fg_status launch_gemm_quant(const uint8_t* a, const float* sa, const uint8_t* b,
                                const float* sb, uint8_t* q, float* s, int64_t M, int64_t N,

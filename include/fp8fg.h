@@ -179,6 +179,37 @@ fp8fg_status fp8_blockscaled_gemm_ws(const uint8_t* a, const float* sa, const ui
 size_t fp8_blockscaled_gemm_workspace_bytes(int64_t M, int64_t N, int64_t K, unsigned flags);
 
 /*
+ * fp8_blockscaled_gemm_noalloc -- fp8_blockscaled_gemm_ws for callers that
+ * cannot allocate device memory when they call the GEMM: code running while a
+ * memory pool is locked or a graph is being captured, allocators that must not
+ * be re-entered, runtimes with a fixed memory budget decided up front.  The
+ * pages have no counterpart of this entry point; it only changes where the
+ * scratch of the stream-K split lives.
+ *
+ * Same operation, arguments, flags (FP8FG_B_TILE1x128, FP8FG_STREAM_K) and
+ * results as fp8_blockscaled_gemm_ws given a large enough workspace; the
+ * caller still passes every input and the output.  The split's partial tiles
+ * go to a 20 MiB array of device memory that the library holds on every GPU
+ * that loads it, until the process exits (the split needs 128 KB per SM, so
+ * it covers devices of up to 160 SMs).  Nothing is allocated: no cudaMalloc,
+ * no cudaFree, no allocating library call.
+ *
+ * - The first call on each device looks up the array's device address
+ *   (cudaGetSymbolAddress) with that device current; make that first call
+ *   before any stream capture.
+ * - Every call shares the array and it keeps the last call's contents; no
+ *   part of it needs to start at zero (each SM of a split writes its whole
+ *   slot before the fix-up kernel reads it).  Calls that overlap on the GPU
+ *   (other streams, other threads) race on it: order them on one stream.
+ * - A shape whose split on the current device would need more than the array
+ *   holds (a device with more than 160 SMs): FP8FG_ERR_UNSUPPORTED_SHAPE,
+ *   nothing launched.
+ */
+fp8fg_status fp8_blockscaled_gemm_noalloc(const uint8_t* a, const float* sa, const uint8_t* b,
+                                          const float* sb, void* c, fp8fg_dtype c_dtype, int64_t M,
+                                          int64_t N, int64_t K, unsigned flags, void* stream);
+
+/*
  * fp8_blockscaled_gemm_quant -- fp8_blockscaled_gemm whose FP32 result is
  * quantised in the epilogue into 1x128 E4M3 tiles along N, the form in which
  * the next FP8 GEMM takes its activation input.  Source: page 2, fine-grained
