@@ -139,6 +139,15 @@ __device__ __forceinline__ void bulk_wait_all() {
 }
 // Order this thread's generic-proxy shared-memory writes before later
 // async-proxy (TMA) reads of them.
+// Programmatic dependent launch: let the launch queued after this one (when
+// it was launched with programmatic stream serialisation) start as SMs free
+// up; and wait until the grids this one overlaps have completed and their
+// writes are visible.
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }

@@ -150,15 +150,16 @@ __host__ __device__ __forceinline__ void sk_share(int i, int n, int nkb, int& kb
   kb1 = static_cast<int>(static_cast<long long>(i + 1) * nkb / n);
 }
 
-// The sequence of units of this CTA, the same for every warp role.  Only the
-// dense kernels that store C (SK) split tiles; the others take whole tiles
-// round-robin.
+// The sequence of units of this CTA, the same for every warp role.  A launch
+// without SK takes the whole tiles [0, dp_tiles) round-robin; the split launch
+// of a dense GEMM that stores C (SK) takes only its CTA's share of one of the
+// tiles after them.
 template <bool SK>
 struct WorkList {
   int next_dp;
   bool sk_pending;
   __device__ __forceinline__ void init(const GemmParams& p) {
-    next_dp = blockIdx.x;
+    next_dp = SK ? INT32_MAX : static_cast<int>(blockIdx.x);
     sk_pending = SK && static_cast<int>(blockIdx.x) < p.sk_grid && p.sk_tiles > 0;
   }
   __device__ __forceinline__ bool next(const GemmParams& p, int num_tiles, Work& w) {
@@ -278,7 +279,7 @@ __device__ __forceinline__ Tile tile_of(int t, const GemmParams& p, const S& sm)
   return r;
 }
 
-template <bool GROUPED, bool BTILE, int EPI>
+template <bool GROUPED, bool BTILE, int EPI, bool SK = false>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     blockscaled_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                             const __grid_constant__ CUtensorMap tmB,
@@ -287,7 +288,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   // 1024-byte alignment of the operand stages (required by the 128B swizzle)
   using Smem = SmemT<GROUPED, BTILE>;
-  constexpr bool SKOK = !GROUPED && EPI == EPI_STORE;   // may split slices (stream-K)
+  // SK: the split launch of a stream-K GEMM (dense kernels that store C
+  // only).  It runs after the launch of the whole tiles, which lets it start
+  // as soon as each of its CTAs leaves (programmatic dependent launch); that
+  // launch's loops keep the slice bounds 0..nkb of a kernel without the split.
+  constexpr bool SKOK = SK && !GROUPED && EPI == EPI_STORE;
+  if constexpr (!GROUPED && EPI == EPI_STORE && !SK) griddep_launch_dependents();
   Smem& sm = *reinterpret_cast<Smem*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
 
@@ -928,6 +934,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     tc_fence_after();
     tmem_dealloc(tmem_base, TMEM_COLS);
   }
+  // the split launch ends only after the whole-tile launch it overlaps, so
+  // that work queued after the GEMM sees all of C
+  if constexpr (SKOK) griddep_wait();
 }
 
 // Stream-K fix-up: BM / kFixupRowsPerCta CTAs per split tile.  The tile's
@@ -1032,9 +1041,9 @@ int group_m_tiles(int64_t m_tiles, int64_t K) {
   return static_cast<int>(g < 1 ? 1 : g);
 }
 
-template <bool GROUPED, bool BTILE, int EPI = EPI_STORE>
+template <bool GROUPED, bool BTILE, int EPI = EPI_STORE, bool SK = false>
 cudaError_t set_smem_attr() {
-  return set_max_dynamic_smem<blockscaled_gemm_kernel<GROUPED, BTILE, EPI>>(
+  return set_max_dynamic_smem<blockscaled_gemm_kernel<GROUPED, BTILE, EPI, SK>>(
       static_cast<int>(smem_bytes<GROUPED, BTILE>()));
 }
 
@@ -1098,10 +1107,6 @@ fp8fg_status launch_gemm(const uint8_t* a, const float* sa, const uint8_t* b, co
   CUtensorMap mA, mB, mC, mW;
   if (!make_maps(&mA, &mB, a, M, b, 0, N, K) || !make_c_map(&mC, c, ct, M, N))
     return FP8FG_ERR_CUDA;
-  if ((b_tile ? set_smem_attr<false, true>()
-              : whole_k ? set_smem_attr<false, false, EPI_WHOLEK>() : set_smem_attr<false, false>()) !=
-      cudaSuccess)
-    return FP8FG_ERR_CUDA;
   GemmParams p{};
   p.sa = sa;
   p.sb = sb;
@@ -1133,16 +1138,51 @@ fp8fg_status launch_gemm(const uint8_t* a, const float* sa, const uint8_t* b, co
     mW = mC;                         // unused
   }
   const int grid = plan.grid;
-  if (b_tile)
-    blockscaled_gemm_kernel<false, true, EPI_STORE>
-        <<<grid, NUM_THREADS, smem_bytes<false, true>(), st>>>(mA, mB, mC, mW, p);
-  else if (whole_k)
+  const bool split = plan.sk_tiles > 0;
+  cudaError_t attr = whole_k  ? set_smem_attr<false, false, EPI_WHOLEK>()
+                     : b_tile ? set_smem_attr<false, true>()
+                              : set_smem_attr<false, false>();
+  if (attr == cudaSuccess && split)
+    attr = b_tile ? set_smem_attr<false, true, EPI_STORE, true>()
+                  : set_smem_attr<false, false, EPI_STORE, true>();
+  if (attr != cudaSuccess) return FP8FG_ERR_CUDA;
+  if (whole_k) {
     blockscaled_gemm_kernel<false, false, EPI_WHOLEK>
         <<<grid, NUM_THREADS, smem_bytes<false, false>(), st>>>(mA, mB, mC, mW, p);
-  else
-    blockscaled_gemm_kernel<false, false, EPI_STORE>
-        <<<grid, NUM_THREADS, smem_bytes<false, false>(), st>>>(mA, mB, mC, mW, p);
-  if (cudaGetLastError() != cudaSuccess) return FP8FG_ERR_CUDA;
+    return cudaGetLastError() == cudaSuccess ? FP8FG_OK : FP8FG_ERR_CUDA;
+  }
+  // whole tiles first; with a split, the tiles after them in a second launch
+  // that may start on each SM as the first launch's CTA there leaves
+  const bool whole = plan.dp_tiles > 0;
+  if (whole) {
+    if (b_tile)
+      blockscaled_gemm_kernel<false, true, EPI_STORE>
+          <<<grid, NUM_THREADS, smem_bytes<false, true>(), st>>>(mA, mB, mC, mW, p);
+    else
+      blockscaled_gemm_kernel<false, false, EPI_STORE>
+          <<<grid, NUM_THREADS, smem_bytes<false, false>(), st>>>(mA, mB, mC, mW, p);
+    if (cudaGetLastError() != cudaSuccess) return FP8FG_ERR_CUDA;
+  }
+  if (split) {
+    cudaLaunchAttribute pdl[1];
+    pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    pdl[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(static_cast<unsigned>(plan.grid));
+    cfg.blockDim = dim3(NUM_THREADS);
+    cfg.dynamicSmemBytes = b_tile ? smem_bytes<false, true>() : smem_bytes<false, false>();
+    cfg.stream = st;
+    // overlap only a launch of this GEMM: without one, the split launch
+    // waits for all earlier work like any other launch
+    cfg.attrs = whole ? pdl : nullptr;
+    cfg.numAttrs = whole ? 1 : 0;
+    const cudaError_t e =
+        b_tile ? cudaLaunchKernelEx(&cfg, blockscaled_gemm_kernel<false, true, EPI_STORE, true>, mA,
+                                    mB, mC, mW, p)
+               : cudaLaunchKernelEx(&cfg, blockscaled_gemm_kernel<false, false, EPI_STORE, true>,
+                                    mA, mB, mC, mW, p);
+    if (e != cudaSuccess) return FP8FG_ERR_CUDA;
+  }
   if (plan.sk_tiles > 0) {
     const dim3 fgrid(static_cast<unsigned>(plan.sk_tiles), BM / kFixupRowsPerCta);
     if (p.c_f32)
