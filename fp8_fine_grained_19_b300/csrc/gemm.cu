@@ -939,49 +939,64 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   if constexpr (SKOK) griddep_wait();
 }
 
-// Stream-K fix-up: BM / kFixupRowsPerCta CTAs per split tile.  The tile's
-// group of CTAs is recomputed from the same split as in WorkList (members whose
-// share is empty, when the group has more CTAs than slices, wrote nothing); a
-// tile with a single member was stored by it and is skipped.  Otherwise the
+// Stream-K fix-up: one thread per four columns of a row of a split tile,
+// BM * BN / (4 * kFixupThreads) CTAs per tile.  The tile's group of CTAs is
+// recomputed from the same split as in WorkList; a tile with a single member
+// was stored by it and is skipped.  Members whose share is empty (only when a
+// group has more CTAs than slices) wrote nothing and are skipped.  The
 // members' partial sums are added in CTA order (FP32, so the result does not
-// depend on timing) and the tile is written to C, clipped at M and N.
-constexpr int kFixupRowsPerCta = 16;
+// depend on timing), loaded eight at a time so that the loads overlap, and
+// the tile is written to C, clipped at M and N.
+constexpr int kFixupThreads = 256;
+constexpr int kFixupCtasPerTile = BM * BN / 4 / kFixupThreads;
+static_assert(kFixupCtasPerTile * kFixupThreads * 4 == BM * BN, "fix-up covers the tile");
 
 template <bool F32OUT>
-__global__ void __launch_bounds__(256) streamk_fixup_kernel(const float* __restrict__ ws,
-                                                            void* __restrict__ c, const GemmParams p) {
+__global__ void __launch_bounds__(kFixupThreads) streamk_fixup_kernel(const float* __restrict__ ws,
+                                                                      void* __restrict__ c,
+                                                                      const GemmParams p) {
   const int j = blockIdx.x;
   const int R = p.sk_tiles, G = p.sk_grid;
   const int f = sk_first_cta(j, R, G), n = sk_first_cta(j + 1, R, G) - f;
   if (n == 1) return;
   const Tile tl = dense_tile(p.dp_tiles + j, p);
-  const int cg = (threadIdx.x & 63) * 4;             // four columns of the tile
-  const int r0 = blockIdx.y * kFixupRowsPerCta;
-  for (int r = r0 + (threadIdx.x >> 6); r < r0 + kFixupRowsPerCta; r += 4) {
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int i = 0; i < n; ++i) {
-      int kb0, kb1;
-      sk_share(i, n, p.nkb, kb0, kb1);
-      if (kb0 == kb1) continue;
-      const float4 v = __ldg(reinterpret_cast<const float4*>(
-          ws + (static_cast<long long>(f + i) * BM + r) * BN + cg));
-      acc.x = __fadd_rn(acc.x, v.x);
-      acc.y = __fadd_rn(acc.y, v.y);
-      acc.z = __fadd_rn(acc.z, v.z);
-      acc.w = __fadd_rn(acc.w, v.w);
+  const int idx = blockIdx.y * kFixupThreads + threadIdx.x;   // float4 of the tile
+  const int r = idx / (BN / 4), cg = (idx % (BN / 4)) * 4;
+  const int row = tl.m0 + r, col = tl.n0 + cg;
+  if (row >= p.M || col >= p.N) return;       // N % 16 == 0: four columns are in or out together
+  const float4* src =
+      reinterpret_cast<const float4*>(ws + (static_cast<long long>(f) * BM + r) * BN + cg);
+  constexpr long long kSlot4 = static_cast<long long>(BM) * BN / 4;   // one member's slot
+  const bool may_be_empty = n > p.nkb;        // else every share holds a slice
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int i0 = 0; i0 < n; i0 += 8) {
+    float4 v[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u)
+      v[u] = i0 + u < n ? __ldg(src + (i0 + u) * kSlot4) : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      if (i0 + u >= n) break;
+      if (may_be_empty) {
+        int kb0, kb1;
+        sk_share(i0 + u, n, p.nkb, kb0, kb1);
+        if (kb0 == kb1) continue;
+      }
+      acc.x = __fadd_rn(acc.x, v[u].x);
+      acc.y = __fadd_rn(acc.y, v[u].y);
+      acc.z = __fadd_rn(acc.z, v[u].z);
+      acc.w = __fadd_rn(acc.w, v[u].w);
     }
-    const int row = tl.m0 + r, col = tl.n0 + cg;
-    if (row >= p.M || col >= p.N) continue;           // N % 16 == 0: four columns are in or out together
-    if constexpr (F32OUT) {
-      *reinterpret_cast<float4*>(static_cast<float*>(c) + static_cast<long long>(row) * p.N + col) = acc;
-    } else {
-      const __nv_bfloat162 lo2 = __floats2bfloat162_rn(acc.x, acc.y);
-      const __nv_bfloat162 hi2 = __floats2bfloat162_rn(acc.z, acc.w);
-      uint2 v;
-      v.x = *reinterpret_cast<const uint32_t*>(&lo2);
-      v.y = *reinterpret_cast<const uint32_t*>(&hi2);
-      *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(c) + static_cast<long long>(row) * p.N + col) = v;
-    }
+  }
+  if constexpr (F32OUT) {
+    *reinterpret_cast<float4*>(static_cast<float*>(c) + static_cast<long long>(row) * p.N + col) = acc;
+  } else {
+    const __nv_bfloat162 lo2 = __floats2bfloat162_rn(acc.x, acc.y);
+    const __nv_bfloat162 hi2 = __floats2bfloat162_rn(acc.z, acc.w);
+    uint2 v;
+    v.x = *reinterpret_cast<const uint32_t*>(&lo2);
+    v.y = *reinterpret_cast<const uint32_t*>(&hi2);
+    *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(c) + static_cast<long long>(row) * p.N + col) = v;
   }
 }
 
@@ -1184,11 +1199,11 @@ fp8fg_status launch_gemm(const uint8_t* a, const float* sa, const uint8_t* b, co
     if (e != cudaSuccess) return FP8FG_ERR_CUDA;
   }
   if (plan.sk_tiles > 0) {
-    const dim3 fgrid(static_cast<unsigned>(plan.sk_tiles), BM / kFixupRowsPerCta);
+    const dim3 fgrid(static_cast<unsigned>(plan.sk_tiles), kFixupCtasPerTile);
     if (p.c_f32)
-      streamk_fixup_kernel<true><<<fgrid, 256, 0, st>>>(static_cast<const float*>(ws), c, p);
+      streamk_fixup_kernel<true><<<fgrid, kFixupThreads, 0, st>>>(static_cast<const float*>(ws), c, p);
     else
-      streamk_fixup_kernel<false><<<fgrid, 256, 0, st>>>(static_cast<const float*>(ws), c, p);
+      streamk_fixup_kernel<false><<<fgrid, kFixupThreads, 0, st>>>(static_cast<const float*>(ws), c, p);
     if (cudaGetLastError() != cudaSuccess) return FP8FG_ERR_CUDA;
   }
   return FP8FG_OK;
