@@ -92,7 +92,7 @@ constexpr int64_t kGroupABytes = int64_t{48} << 20;
 constexpr int MAX_EXPERTS = 1024;
 constexpr int SCALE_WARP = 10;        // tile mode: loads and transposes the B column scales
 constexpr int SB = 4;                 // tile mode: slices per scale-ring slot
-constexpr int SB_SLOTS = 3;           // tile mode: scale-ring slots
+constexpr int SB_SLOTS = 2;           // tile mode: scale-ring slots
 constexpr int CST_BYTES = 2048;       // output staging per promotion warp: 32 rows x 64 bytes
 constexpr int CST_ROW = 64;           // bytes per staged row (the tensor map's 64-byte swizzle)
 constexpr uint32_t IDESC = idesc_e4m3_f32(BM, BN);
@@ -194,8 +194,10 @@ struct SmemT {
   uint8_t b[STAGES][B_BYTES];
   // output staging of the promotion warps: warp w stages in bytes [2 KB w, 2 KB (w+1))
   alignas(1024) uint8_t cst[NUM_EPI_WARPS][CST_BYTES];
-  // tile mode: the B column scales of SB slices of the current tile, [slice][column]
+  // tile mode: the B column scales of SB slices of the current tile, [slice][column],
+  // and the A row scales of the same slices, [slice][row]
   float sring[BTILE ? SB_SLOTS : 1][BTILE ? SB : 1][BTILE ? BN : 1];
+  float saring[BTILE ? SB_SLOTS : 1][BTILE ? SB : 1][BTILE ? BM : 1];
   uint64_t full_bar[STAGES];
   uint64_t empty_bar[STAGES];
   uint64_t tfull_bar[2];
@@ -473,7 +475,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       // For every SB slices of a tile, the 256 column scales sb[n0 + c, kb]
       // (c = lane + 32 i) are read and written transposed, [slice][column],
       // into a ring slot that the promotion warps read as 16-byte column
-      // pairs.  Columns past N read the last column's scales (never stored).
+      // pairs, and the 128 row scales sa[m0 + r, kb] likewise, [slice][row].
+      // Columns past N and rows past M read the last column's and row's
+      // scales (never stored).
       uint32_t grp = 0;
       bool live = true;
       WorkList<SKOK> wl;
@@ -495,6 +499,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
             for (int q = 0; q < SB; ++q)
               sm.sring[slot][q][c] = kb0 + q < wk.kb1 ? __ldg(col + kb0 + q) : 0.0f;
+          }
+#pragma unroll
+          for (int i = 0; i < BM / 32; ++i) {
+            const int r = lane + 32 * i;
+            const float* rw = p.sa + static_cast<int64_t>(min(tl.m0 + r, p.M - 1)) * nkb;
+#pragma unroll
+            for (int q = 0; q < SB; ++q)
+              sm.saring[slot][q][r] = kb0 + q < wk.kb1 ? __ldg(rw + kb0 + q) : 0.0f;
           }
           __syncwarp();
           if (lane == 0) mbar_arrive(smem_u32(&sm.sfull_bar[slot]));
@@ -536,11 +548,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       for (int j = 0; j < 64; ++j) acc[j] = 0;
 
       if constexpr (BTILE) {
-        // Column scales come from the scale warp's ring: each slot holds SB
-        // slices of this tile's 256 columns; a warp waits for a slot before
-        // its first slice and frees it after its last, so no barrier joins
-        // the promotion warps.
-        float sa_next = __ldg(sa_row + wk.kb0);
+        // Row and column scales come from the scale warp's ring: each slot
+        // holds SB slices of this tile's 128 row and 256 column scales; a warp
+        // waits for a slot before its first slice and frees it after its
+        // last, so no barrier joins the promotion warps and they issue no
+        // global loads.
         for (int kb = wk.kb0; kb < wk.kb1; ++kb, ++it) {
           const uint32_t slot = sgrp % SB_SLOTS;
           const int g = kb - wk.kb0;                  // slice within the unit (ring groups start at kb0)
@@ -549,8 +561,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             ok = false;
             break;
           }
-          const float sa_cur = sa_next;
-          if (kb + 1 < wk.kb1) sa_next = __ldg(sa_row + kb + 1);
+          const float sa_cur = sm.saring[slot][g % SB][quad * 32 + lane];
           const uint32_t buf = it & 1, bpar = (it >> 1) & 1;
           if (!mbar_wait(smem_u32(&sm.tfull_bar[buf]), bpar, p.wait_limit, abort_flag, p.status)) {
             ok = false;
@@ -560,23 +571,27 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           const uint32_t taddr = lane_taddr + buf * BN;
           const uint64_t sa2 = pack2(__float_as_uint(sa_cur), __float_as_uint(sa_cur));
           const uint32_t sbv = smem_u32(&sm.sring[slot][g % SB][half * 128]);
+          // Eight chunks of 16 columns, software-pipelined: chunk c + 1's TMEM
+          // load is in flight while chunk c's FMAs issue, and each chunk's
+          // coefficients sa * sb[col] (scales read as column pairs) are formed
+          // before its wait.
+          uint32_t r[2][16];
+          tmem_ld_16cols(taddr, r[0]);
 #pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            // the coefficients sa * sb[col] of this chunk are formed while its
-            // TMEM load is in flight; the scales are read as column pairs
-            uint32_t r[32];
-            tmem_ld_32cols(taddr + c * 32, r);
-            uint64_t cf[16];
+          for (int c = 0; c < 8; ++c) {
+            uint64_t cf[8];
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
+            for (int j = 0; j < 4; ++j) {
               uint64_t q0, q1;
-              lds_2x64(sbv + (c * 32 + 4 * j) * 4, q0, q1);
+              lds_2x64(sbv + (c * 16 + 4 * j) * 4, q0, q1);
               cf[2 * j] = mul2_s(q0, sa2);
               cf[2 * j + 1] = mul2_s(q1, sa2);
             }
-            tmem_ld_wait();
+            tmem_ld_wait_regs(r[c & 1]);
+            if (c + 1 < 8) tmem_ld_16cols(taddr + (c + 1) * 16, r[(c + 1) & 1]);
 #pragma unroll
-            for (int j = 0; j < 16; ++j) fma2_s(acc[c * 16 + j], pack2(r[2 * j], r[2 * j + 1]), cf[j]);
+            for (int j = 0; j < 8; ++j)
+              fma2_s(acc[c * 8 + j], pack2(r[c & 1][2 * j], r[c & 1][2 * j + 1]), cf[j]);
           }
           tc_fence_before();
           __syncwarp();
