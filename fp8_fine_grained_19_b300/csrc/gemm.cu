@@ -572,20 +572,22 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           const uint64_t sa2 = pack2(__float_as_uint(sa_cur), __float_as_uint(sa_cur));
           const uint32_t sbv = smem_u32(&sm.sring[slot][g % SB][half * 128]);
           // Eight chunks of 16 columns, software-pipelined: chunk c + 1's TMEM
-          // load is in flight while chunk c's FMAs issue, and each chunk's
-          // coefficients sa * sb[col] (scales read as column pairs) are formed
-          // before its wait.
+          // load and column scales (read as pairs) are in flight while chunk
+          // c's coefficients sa * sb[col] and FMAs issue.
           uint32_t r[2][16];
+          uint64_t q[8];
           tmem_ld_16cols(taddr, r[0]);
+#pragma unroll
+          for (int j = 0; j < 4; ++j) lds_2x64(sbv + 16 * j, q[2 * j], q[2 * j + 1]);
 #pragma unroll
           for (int c = 0; c < 8; ++c) {
             uint64_t cf[8];
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              uint64_t q0, q1;
-              lds_2x64(sbv + (c * 16 + 4 * j) * 4, q0, q1);
-              cf[2 * j] = mul2_s(q0, sa2);
-              cf[2 * j + 1] = mul2_s(q1, sa2);
+            for (int j = 0; j < 8; ++j) cf[j] = mul2_s(q[j], sa2);
+            if (c + 1 < 8) {
+#pragma unroll
+              for (int j = 0; j < 4; ++j)
+                lds_2x64(sbv + ((c + 1) * 16 + 4 * j) * 4, q[2 * j], q[2 * j + 1]);
             }
             tmem_ld_wait_regs(r[c & 1]);
             if (c + 1 < 8) tmem_ld_16cols(taddr + (c + 1) * 16, r[(c + 1) & 1]);
