@@ -615,6 +615,16 @@ def run_workload(args, rank, world):
                 Nf, Kh, Mt, fp8.B_TILE1x128, cur()), "wgrad"),
              "tensor", 2 * Nf * Kh * Mt),
         ]
+        # torch's own kernels moving the same bytes, timed in a separate loop: the
+        # floor a kernel of this size reaches (launch ramp and tail included)
+        dy_e4m3 = torch.empty((Mt, Nf), dtype=torch.float8_e4m3fn, device=dev)
+        qx_copy = torch.empty_like(qx)
+        compare_ops = [
+            ("floor_cast_dY_bf16_to_e4m3", lambda: dy_e4m3.copy_(dy), "hbm", Mt * Nf * 3),
+            ("floor_copy_X_codes", lambda: qx_copy.copy_(qx), "hbm", Mt * Kh * 2),
+        ]
+        floors = {"act_quant_dY": "floor_cast_dY_bf16_to_e4m3", "act_quant_T_dY": "floor_cast_dY_bf16_to_e4m3",
+                  "requant_T_X_stored": "floor_copy_X_codes"}
         desc = {"workload": "backward_ffn_dy4096x18432_x4096x7168_w18432x7168",
                 "step": "act_quant dY (1x128) + 128x1 quant of dY + 128x1 re-quantisation of the stored "
                         "FP8 X + weight_quant W with W^T + Dgrad dY.W -> bf16 [4096,7168] (stream-K split "
@@ -774,7 +784,7 @@ def run_workload(args, rank, world):
                                         world)
     fp8_peak, peak_source, fp8_burst, fp8_sustained = fp8_peaks(pk, total_ms)
     extra = []
-    if args.workload == "moe":
+    if args.workload in ("moe", "backward"):
         _, per_c, _ = _timed_loop([(n, f) for n, f, _, _ in compare_ops], max(steps // 4, 5), args.warmup,
                                   stream, dev, world)
         per.update(per_c)
@@ -802,6 +812,14 @@ def run_workload(args, rank, world):
                 t_tc = flops[name] / (fp8_peak * 1e12) * 1e3
                 per_op[name].update({"TFLOP/s": round(tf, 2), "roofline_ms": round(max(t_mem, t_tc), 5),
                                      "frac_of_roofline": round(max(t_mem, t_tc) / ms, 4)})
+    if args.workload == "backward":
+        cfg_floor = ("quantiser ramp floors: torch's BF16->E4M3 cast of dY and copy of the stored X codes, "
+                     "timed in a separate loop (per_op floor_*, and ramp_floor beside each quantiser)")
+        for name, fl in floors.items():
+            per_op[name]["ramp_floor"] = {
+                "what": f"per_op {fl}: torch moving the same bytes (separate loop)",
+                "ms": per_op[fl]["ms"], "GB/s": per_op[fl]["GB/s"],
+                "frac_of_floor": round(per_op[fl]["ms"] / per_op[name]["ms"], 4)}
     dom = max(ops, key=lambda o: per[o[0]])
     dname, _, dkind, damount = dom
     if dkind == "tensor":
@@ -816,6 +834,8 @@ def run_workload(args, rank, world):
                 "frac": round(ach / hbm, 4), "peak_source": f"copy bandwidth, {pk['source']}",
                 "traffic": None, "algorithmic_bytes": damount}
     cfg = dict(desc)
+    if args.workload == "backward":
+        cfg["floors"] = cfg_floor
     cfg["parallelism"] = f"{world} independent replica(s)"
     cfg["timing"] = ("every op replayed from its own CUDA graph; the timed region is enqueued behind a "
                      "GPU-side wait, so the host is ahead of the GPU and per-op times are kernel times")
