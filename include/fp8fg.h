@@ -158,6 +158,13 @@ fp8fg_status fp8_blockscaled_gemm(const uint8_t* a, const float* sa, const uint8
  * one more FP32 addition per extra part than the whole-tile path).
  * FP8FG_STREAM_K applies the split whenever the tiles do not fill whole waves.
  *
+ * A split call enqueues up to three kernels on `stream`: the whole tiles; the
+ * shared tiles, launched with programmatic stream serialisation so that they
+ * start on each SM as the first kernel's block there finishes (they read only
+ * the inputs, and end only after the first kernel has); the fix-up.  Work
+ * enqueued after the call sees all of C, as after any other call; the three
+ * launches can be captured into a CUDA graph like a single one.
+ *
  * workspace  DEVICE, 16-byte aligned, at least
  *            fp8_blockscaled_gemm_workspace_bytes(M, N, K, flags) bytes (the
  *            split needs 128 KB per SM of the current device: 18.5 MB on 148
