@@ -93,3 +93,52 @@ def test_auto_split_on_the_dgrad_shape(cuda_lib):
     assert cuda_lib.gemm_workspace_bytes(4096, 7168, 18432) > 0
     # the Fprop shape's last wave is nearly full: no split
     assert cuda_lib.gemm_workspace_bytes(4096, 18432, 7168) == 0
+
+
+def test_split_inside_a_cuda_graph(cuda_lib):
+    # 160 output tiles on 148 SMs: a whole-tile launch and a split launch (the
+    # second queued with programmatic stream serialisation), then the fix-up.
+    # In one captured graph: act_quant produces A, the GEMM consumes it, and a
+    # torch op reads C right after; every replay must equal the eager run.
+    M, N, K = 2048, 2560, 1280
+    lib = cuda_lib.load()
+    g = torch.Generator(device="cuda")
+    g.manual_seed(11)
+    x = torch.randn((M, K), generator=g, device="cuda").to(torch.bfloat16)
+    _, _, qb_np, sb_np = _operands(M, N, K, 12)
+    qb, sb = H.to_dev(qb_np), H.to_dev(sb_np)
+    qa = torch.empty((M, K), dtype=torch.uint8, device="cuda")
+    sa = torch.empty((M, K // 128), dtype=torch.float32, device="cuda")
+    need = cuda_lib.gemm_workspace_bytes(M, N, K, stream_k=True)
+    assert need > 0
+    ws = torch.empty(need, dtype=torch.uint8, device="cuda")
+    c = torch.empty((M, N), dtype=torch.float32, device="cuda")
+    y = torch.empty_like(c)
+
+    def body():
+        sp = torch.cuda.current_stream().cuda_stream
+        assert lib.fp8_act_quant(x.data_ptr(), cuda_lib.BF16, M, K, qa.data_ptr(), sa.data_ptr(), 0,
+                                 sp) == cuda_lib.OK
+        assert lib.fp8_blockscaled_gemm_ws(qa.data_ptr(), sa.data_ptr(), qb.data_ptr(), sb.data_ptr(),
+                                           c.data_ptr(), cuda_lib.F32, M, N, K, cuda_lib.STREAM_K,
+                                           ws.data_ptr(), need, sp) == cuda_lib.OK
+        torch.mul(c, 2.0, out=y)
+
+    body()
+    torch.cuda.synchronize()
+    c_eager, y_eager = c.clone(), y.clone()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        body()
+    for _ in range(2):
+        c.fill_(float("nan"))
+        y.fill_(float("nan"))
+        qa.zero_()
+        graph.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(c, c_eager) and torch.equal(y, y_eager)
+    assert cuda_lib.device_status() == cuda_lib.OK
+    qa_np, sa_np = qa.cpu().numpy(), sa.cpu().numpy()
+    ref = oracle.gemm(qa_np, sa_np, qb_np, sb_np)
+    H.assert_elementwise(c_eager, ref, H.gemm_error_bound(qa_np, sa_np, qb_np, sb_np, extra_adds=K // 128),
+                         "split in a graph")
