@@ -640,6 +640,7 @@ def run_workload(args, rank, world):
         return torch.empty(shape, dtype=torch.float32, device=dev)
 
     # each op: (name, fn, kind, amount) with kind "hbm" (algorithmic bytes) or "tensor" (FLOPs)
+    extra_launches = 0                 # launches of ours beyond one per op
     ops = []
     desc = {}
     if args.workload == "backward":
@@ -694,6 +695,8 @@ def run_workload(args, rank, world):
             ("floor_cast_dY_bf16_to_e4m3", lambda: dy_e4m3.copy_(dy), "hbm", Mt * Nf * 3),
             ("floor_copy_X_codes", lambda: qx_copy.copy_(qx), "hbm", Mt * Kh * 2),
         ]
+        # Dgrad with the split is three launches: whole tiles, split tiles, fix-up
+        extra_launches = 2 if ws_dgrad is not None else 0
         floors = {"act_quant_dY": "floor_cast_dY_bf16_to_e4m3", "act_quant_T_dY": "floor_cast_dY_bf16_to_e4m3",
                   "requant_T_X_stored": "floor_copy_X_codes"}
         desc = {"workload": "backward_ffn_dy4096x18432_x4096x7168_w18432x7168",
@@ -916,7 +919,7 @@ def run_workload(args, rank, world):
         "ms_per_step": round(total_ms / steps, 5), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "e4m3 x e4m3 -> f32 accumulate", "data": "synthetic",
         "config": cfg, "roofline": roof, "per_op": per_op, "e2e": None,
-        "gpu_launches": len(ops) * steps, "clocks": clocks,
+        "gpu_launches": (len(ops) + extra_launches) * steps, "clocks": clocks,
     }
 
 
