@@ -77,6 +77,24 @@ cudaError_t set_max_dynamic_smem(int bytes) {
   return e;
 }
 
+// CTAs of `Kernel` that one SM of the current device holds at once, launched
+// with `threads` threads and `smem` bytes of dynamic shared memory (each kernel
+// is always launched with one such shape); at least 1, cached per device.  A
+// persistent grid larger than this would leave its last CTAs waiting for SMs.
+template <auto Kernel>
+int resident_ctas_per_sm(int threads, int smem) {
+  static std::atomic<int> cache[kMaxDevices] = {};
+  const int d = current_device();
+  if (d < 0) return 1;
+  int occ = cache[d].load(std::memory_order_acquire);
+  if (occ > 0) return occ;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, Kernel, threads, smem) != cudaSuccess ||
+      occ < 1)
+    occ = 1;
+  cache[d].store(occ, std::memory_order_release);
+  return occ;
+}
+
 // Encode a tensor map (innermost dimension first, zero fill); returns false if
 // the driver rejects it.
 bool encode_tensor_map(CUtensorMap* map, CUtensorMapDataType dtype, const void* base, int rank,

@@ -142,8 +142,9 @@ __global__ void __launch_bounds__(256) act_quant_rows_kernel(const T* __restrict
 // --------------------------------------------------------------------------
 // 128x1 tiles along M, transposed output.  Persistent CTAs walk blocks of 128
 // rows x COLS columns of x (COLS = 128 for BF16, 64 for FP32: 32 KB either
-// way); TMA fills a 2-stage ring of such blocks in shared memory (3 CTAs of 512
-// threads per SM), so the threads only read columns, convert and store.
+// way); TMA fills a 2-stage ring of such blocks in shared memory, so the
+// threads only read columns, convert and store.  The grid is the CTAs of 512
+// threads the SMs hold at once (two per SM for BF16, three for FP32).
 // Thread (j, g) owns the column
 // pair (2j, 2j+1) and rows g*RPG.. of the block: it reads them as 32- or 64-bit
 // words (conflict-free: a block row is 256 contiguous bytes), publishes its two
@@ -567,22 +568,24 @@ cudaError_t launch_act_quant_cols(const void* x, fp8fg_dtype xt, int64_t M, int6
                          x, 2, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_NONE))
     return cudaErrorInvalidValue;
   const int64_t n_tiles = (K / cols) * (M / 128);
-  const int64_t max_ctas = static_cast<int64_t>(device_sm_count()) * 3;   // 3 x 64 KB per SM
-  const int grid = static_cast<int>(n_tiles < max_ctas ? n_tiles : max_ctas);
   const int smem = kColStages * 32768;
-  if (bf16) {
-    const cudaError_t attr = set_max_dynamic_smem<act_quant_cols_kernel<__nv_bfloat16>>(smem);
-    if (attr != cudaSuccess) return attr;
+  // persistent: exactly the CTAs the SMs hold at once (two per SM with the
+  // 64 KB ring and the static staging), so that no CTA waits for an SM
+  const cudaError_t attr = bf16 ? set_max_dynamic_smem<act_quant_cols_kernel<__nv_bfloat16>>(smem)
+                                : set_max_dynamic_smem<act_quant_cols_kernel<float>>(smem);
+  if (attr != cudaSuccess) return attr;
+  const int per_sm = bf16 ? resident_ctas_per_sm<act_quant_cols_kernel<__nv_bfloat16>>(kColThreads, smem)
+                          : resident_ctas_per_sm<act_quant_cols_kernel<float>>(kColThreads, smem);
+  const int64_t max_ctas = static_cast<int64_t>(device_sm_count()) * per_sm;
+  const int grid = static_cast<int>(n_tiles < max_ctas ? n_tiles : max_ctas);
+  if (bf16)
     act_quant_cols_kernel<__nv_bfloat16><<<grid, kColThreads, smem, st>>>(
         map, qt, st_, static_cast<int>(M), static_cast<int>(K), pow2 ? 1 : 0, wait_limit_cycles(),
         device_status_word());
-  } else {
-    const cudaError_t attr = set_max_dynamic_smem<act_quant_cols_kernel<float>>(smem);
-    if (attr != cudaSuccess) return attr;
+  else
     act_quant_cols_kernel<float><<<grid, kColThreads, smem, st>>>(
         map, qt, st_, static_cast<int>(M), static_cast<int>(K), pow2 ? 1 : 0, wait_limit_cycles(),
         device_status_word());
-  }
   return cudaGetLastError();
 }
 
