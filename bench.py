@@ -472,12 +472,13 @@ def run_ours(args, rank, world):
     return out
 
 
-def vendor_context(ours, qa, sa, qb, sb, c, stream):
+def vendor_context(ours, qa, sa, qb, sb, c, stream, block=True, reps=10):
     """cuBLASLt's FP8 GEMM (torch._scaled_mm) on the same codes, timed in one
     loop with ours (idle gap before every launch, so both see the same clock).
     Context only: per-tensor scales skip the fine-grained promotion; the
-    block-scaled form (1x128 A scales, 128x128 B scales) is tried if this
-    torch accepts it, and its output is compared with ours."""
+    block-scaled form (1x128 A scales, 128x128 B scales; `block`) is tried if
+    this torch accepts it, and its output is compared with ours.  The output
+    has c's dtype."""
     import statistics
 
     import torch
@@ -486,16 +487,17 @@ def vendor_context(ours, qa, sa, qb, sb, c, stream):
     N = qb.shape[0]
     a8, b8 = qa.view(torch.float8_e4m3fn), qb.view(torch.float8_e4m3fn)
     one = torch.ones((), device=qa.device, dtype=torch.float32)
-    res = {"what": "torch._scaled_mm (cuBLASLt) on the same E4M3 codes, BF16 out; timed interleaved with "
-                   "ours, an idle gap before each launch; not part of the timed step"}
-    cands = {"per_tensor_scales": lambda: torch._scaled_mm(a8, b8.t(), scale_a=one, scale_b=one,
-                                                           out_dtype=torch.bfloat16)}
+    od = c.dtype
+    res = {"what": f"torch._scaled_mm (cuBLASLt) on the same E4M3 codes, {str(od)[6:]} out; timed "
+                   "interleaved with ours, an idle gap before each launch; not part of the timed step"}
+    cands = {"per_tensor_scales": lambda: torch._scaled_mm(a8, b8.t(), scale_a=one, scale_b=one, out_dtype=od)}
     # block scales as cuBLASLt's 1x128 x 128x128 recipe expects them: A's [M, K/128]
     # and B's [K/128, N/128] (B = qb^T), each tried in both memory orders
-    for name, sa_, sb_ in (("block_scales", sa, sb.t()),
-                           ("block_scales_other_order", sa.t().contiguous().t(), sb.t().contiguous())):
-        cands[name] = (lambda sa_=sa_, sb_=sb_: torch._scaled_mm(a8, b8.t(), scale_a=sa_, scale_b=sb_,
-                                                                 out_dtype=torch.bfloat16))
+    if block:
+        for name, sa_, sb_ in (("block_scales", sa, sb.t()),
+                               ("block_scales_other_order", sa.t().contiguous().t(), sb.t().contiguous())):
+            cands[name] = (lambda sa_=sa_, sb_=sb_: torch._scaled_mm(a8, b8.t(), scale_a=sa_, scale_b=sb_,
+                                                                     out_dtype=od))
     fns = {"ours": ours}
     for name, fn in cands.items():
         try:
@@ -514,7 +516,7 @@ def vendor_context(ours, qa, sa, qb, sb, c, stream):
         except Exception as e:         # noqa: BLE001 - a torch build without this form
             res[name] = {"unavailable": str(e).splitlines()[0][:160]}
     ts = {n: [] for n in fns}
-    for _ in range(10):
+    for _ in range(reps):
         for n, fn in fns.items():
             torch.cuda._sleep(40_000_000)
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -641,6 +643,7 @@ def run_workload(args, rank, world):
 
     # each op: (name, fn, kind, amount) with kind "hbm" (algorithmic bytes) or "tensor" (FLOPs)
     extra_launches = 0                 # launches of ours beyond one per op
+    vendor_jobs = []                   # GEMMs timed beside cuBLASLt's FP8 GEMM after the step
     ops = []
     desc = {}
     if args.workload == "backward":
@@ -697,6 +700,8 @@ def run_workload(args, rank, world):
         ]
         # Dgrad with the split is three launches: whole tiles, split tiles, fix-up
         extra_launches = 2 if ws_dgrad is not None else 0
+        vendor_jobs = [("gemm_dgrad", qd, sd, qwt, swt, dx, True),
+                       ("gemm_wgrad", qdt, sdt, qxt, sxt, dw, False)]   # tile scales on B: per-tensor only
         floors = {"act_quant_dY": "floor_cast_dY_bf16_to_e4m3", "act_quant_T_dY": "floor_cast_dY_bf16_to_e4m3",
                   "requant_T_X_stored": "floor_copy_X_codes"}
         desc = {"workload": "backward_ffn_dy4096x18432_x4096x7168_w18432x7168",
@@ -834,6 +839,8 @@ def run_workload(args, rank, world):
                 qa_, sa_ = u8(Mm, Kk), f32(Mm, Kk // 128)
                 qb_, sb_ = u8(Nn, Kk), f32(Nn // 128, Kk // 128)
                 cc = torch.empty((Mm, Nn), dtype=torch.float32, device=dev)
+                if not fg:
+                    vendor_jobs.append((f"gemm_k{Kk}", qa_, sa_, qb_, sb_, cc, True))
                 fa.append(lambda xx=xx, qa_=qa_, sa_=sa_, Mm=Mm, Kk=Kk: check(lib.fp8_act_quant(
                     xx.data_ptr(), fp8.BF16, Mm, Kk, qa_.data_ptr(), sa_.data_ptr(), 0, cur()), "act_quant"))
                 fw.append(lambda ww=ww, qb_=qb_, sb_=sb_, Nn=Nn, Kk=Kk: check(lib.fp8_weight_quant(
@@ -907,6 +914,11 @@ def run_workload(args, rank, world):
         roof = {"kernel": dname, "bound": "hbm", "achieved": round(ach, 1), "peak": hbm, "unit": "GB/s",
                 "frac": round(ach / hbm, 4), "peak_source": f"copy bandwidth, {pk['source']}",
                 "traffic": None, "algorithmic_bytes": damount}
+    vendor = None
+    if vendor_jobs and not args.no_vendor_context and rank == 0:
+        fnmap = {n: (f[0] if isinstance(f, list) else f) for n, f, _, _ in ops}
+        vendor = {n: vendor_context(fnmap[n], a_, sa_, b_, sb_, c_, stream, block=blk, reps=5)
+                  for n, a_, sa_, b_, sb_, c_, blk in vendor_jobs}
     cfg = dict(desc)
     if args.workload == "backward":
         cfg["floors"] = cfg_floor
@@ -920,6 +932,7 @@ def run_workload(args, rank, world):
         "vs_baseline": None, "dtype": "e4m3 x e4m3 -> f32 accumulate", "data": "synthetic",
         "config": cfg, "roofline": roof, "per_op": per_op, "e2e": None,
         "gpu_launches": (len(ops) + extra_launches) * steps, "clocks": clocks,
+        **({"vendor_context": vendor} if vendor else {}),
     }
 
 
