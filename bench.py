@@ -389,6 +389,36 @@ def run_ours(args, rank, world):
         for cc, ch in zip(cs, c_hs):
             if not (torch.equal(cc, c_ref) and torch.equal(ch, c_ref.cpu())):
                 raise RuntimeError("e2e result differs from the device-resident step")
+        # the host link alone: the same copies without the compute, each way and
+        # both ways at once; the step time they allow bounds the end-to-end rate
+        def link(kind, reps=5):
+            t0_, t1_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            t0_.record(stream)
+            h2d.wait_event(t0_)
+            d2h.wait_event(t0_)
+            for _ in range(reps):
+                if kind in ("h2d", "both"):
+                    with torch.cuda.stream(h2d):
+                        xs[0].copy_(x_h, non_blocking=True)
+                        wss[0].copy_(w_h, non_blocking=True)
+                if kind in ("d2h", "both"):
+                    with torch.cuda.stream(d2h):
+                        c_hs[0].copy_(cs[0], non_blocking=True)
+            stream.wait_stream(h2d)
+            stream.wait_stream(d2h)
+            t1_.record(stream)
+            torch.cuda.synchronize()
+            return t0_.elapsed_time(t1_) / reps
+        hb, db = e2e["h2d_bytes_per_step"], e2e["d2h_bytes_per_step"]
+        t_h, t_d, t_b = link("h2d"), link("d2h"), link("both")
+        e2e["host_link"] = {"h2d_GB/s": round(hb / (t_h * 1e-3) / 1e9, 1),
+                            "d2h_GB/s": round(db / (t_d * 1e-3) / 1e9, 1),
+                            "copies_alone_ms_per_step": round(t_b, 4),
+                            "step_ms": round(ms2 / n2, 4),
+                            "what": "the same pinned copies timed without compute (H2D, D2H, both at once); "
+                                    "copies_alone_ms_per_step is the step time the link allows"}
+        # the step's C again in buffer 0, as the device-resident step left it
+        cs[0].copy_(c_ref)
         del xs[1], wss[1], cs[1], c_ref
 
     vendor = None
