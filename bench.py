@@ -329,8 +329,8 @@ def run_ours(args, rank, world):
     # host memory and reads its C back.  Steps are pipelined the way a training
     # loop runs them: step i+1's inputs travel on a copy stream into the other
     # of two device buffers while step i computes, and results come back on a
-    # third stream (the host link is full duplex); a step's compute waits for its
-    # inputs, and a buffer is refilled only after the step two back released it.
+    # third stream; a step's compute waits for its inputs, and a buffer is
+    # refilled only after the step two back released it.
     e2e = None
     if not args.no_e2e:
         c_ref = c.clone()                                         # C of the device-resident step
