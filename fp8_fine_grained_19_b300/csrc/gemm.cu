@@ -281,6 +281,15 @@ __device__ __forceinline__ Tile tile_of(int t, const GemmParams& p, const S& sm)
   return r;
 }
 
+// Limit of the waits that let a stopping CTA's own TMA copies and MMAs finish
+// before it releases its shared memory and TMEM: at least 2^27 cycles
+// (~67 ms), whatever limit the caller set for the pipeline waits, so that a
+// small limit cannot make a CTA leave with work still landing.
+__device__ __forceinline__ long long teardown_limit(long long wait_limit) {
+  constexpr long long kMin = 1ll << 27;
+  return wait_limit > kMin ? wait_limit : kMin;
+}
+
 template <bool GROUPED, bool BTILE, int EPI, bool SK = false>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     blockscaled_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
@@ -419,7 +428,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         volatile int never = 0;
         for (int s = 0; s < STAGES; ++s)
           if (issued & (1u << s))
-            mbar_wait(smem_u32(&sm.full_bar[s]), (issued_parity >> s) & 1, p.wait_limit, &never,
+            mbar_wait(smem_u32(&sm.full_bar[s]), (issued_parity >> s) & 1, teardown_limit(p.wait_limit), &never,
                       p.status);
       }
     } else if (warp == MMA_WARP) {
@@ -468,7 +477,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       mma_commit_elect(smem_u32(&sm.drain_bar));
       if (lane == 0) {
         volatile int never = 0;
-        mbar_wait(smem_u32(&sm.drain_bar), 0, p.wait_limit, &never, p.status);
+        mbar_wait(smem_u32(&sm.drain_bar), 0, teardown_limit(p.wait_limit), &never, p.status);
       }
     } else if (BTILE && warp == SCALE_WARP) {
       // ----------------------------------------------- tile-mode scale loader

@@ -302,6 +302,9 @@ int fp8fg_abi_version(void);
  * fp8fg_set_wait_limit -- cycle limit of every pipeline wait in later launches
  * (default 2^32 cycles, about two seconds; 0 restores the default).  Also read
  * once from the environment variable FP8FG_WAIT_LIMIT_CYCLES.  Host-side only.
+ * The waits with which a stopping GEMM block lets its own copies and MMAs
+ * finish before it frees its memory use at least 2^27 cycles (~67 ms) even
+ * when a smaller limit is set.
  */
 void fp8fg_set_wait_limit(uint64_t cycles);
 
