@@ -131,6 +131,12 @@ fp8fg_status fp8_weight_quant(const void* w, fp8fg_dtype w_dtype, int64_t N, int
  * output is rounded once (RNE to BF16, or stored as FP32).
  * M >= 0 arbitrary (0: nothing launched); N >= 16; K >= 128.
  *
+ * The dense kernel lets a launch queued after it with programmatic stream
+ * serialisation start early (griddepcontrol.launch_dependents at its start);
+ * such a kernel must wait for it (griddepcontrol.wait, or
+ * cudaGridDependencySynchronize) before it reads C, as programmatic dependent
+ * launch requires.  Launches without that attribute see the usual stream order.
+ *
  * FP8FG_WHOLE_K (study mode, not with FP8FG_B_TILE1x128): the promotion the
  * pages prescribe is switched off.  All of K accumulates inside the tensor
  * core (one TMEM accumulator per tile) and the result is scaled once by
